@@ -1,0 +1,151 @@
+/*
+ * Uniform-grid build oracle: a plain, slow, single-threaded CPU statement of
+ * what the grid build computes, written to be checked against the pages by eye.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the bench's
+ * CPU-baseline (and reference) leg load this library; the product path never
+ * does, and it shares no code, header or table with the CUDA library.
+ *
+ * Sources (the "guia/webgpu" lessons on blog.wandres.dev):
+ *   [count]   "Contar partículas por celda", §El kernel: each particle's cell
+ *             index c is saved in celdaDe[i] and conteos[c] is incremented;
+ *             the range guard (a clamp) lives inside the cell-index helper.
+ *             §Poner a cero: conteos starts every build at zero.
+ *   [scan]    "Construir el índice de la rejilla con un prefix sum",
+ *             §Del conteo al inicio: inicios = exclusive scan of conteos, with
+ *             one extra slot at the end holding the total.
+ *   [scatter] same page, §La dispersión: a per-cell cursor starting at zero
+ *             hands out slots, ordenado[inicios[c] + slot] = i;
+ *             §El orden dentro de la celda: the particle index is the
+ *             tie-break that makes the result reproducible.  Visiting the
+ *             particles in ascending index is that order.
+ *   [reorder] "Reordenar por celda y la coalescencia de memoria",
+ *             §El kernel de reordenación: destino[k] = origen[ordenado[k]]
+ *             (a gather of the whole 32-byte record); §El orden de las celdas:
+ *             the linear cell index is x + y*GX + z*GX*GY.
+ *   [record]  "El estado de las partículas en storage buffers",
+ *             §La estructura y su alineación: Particula is pos (3 floats),
+ *             vida, vel (3 floats), masa — 32 bytes, pos at offset 0.
+ *
+ * Readings where the pages are silent (the helper bodies were not on them):
+ *   - cell coordinate along an axis: floor((p - o) * invCell) in fp32, with
+ *     invCell = 1.0f / cellSize rounded once, each operation rounded to
+ *     nearest and no fused multiply-add (build with -ffp-contract=off);
+ *   - the clamp saturates to [0, dims-1]; NaN and -inf go to 0, +inf to
+ *     dims-1.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_FLOATS_PER_PARTICLE 8
+#define ORACLE_RECORD_BYTES 32
+
+/* [count] Clamped integer cell coordinate along one axis. */
+static uint32_t axis_cell(float p, float o, float invCell, uint32_t dim)
+{
+    float t = p - o;
+    float u = t * invCell;
+    float f = floorf(u);
+    if (isnan(f) || f < 0.0f)
+        return 0u;
+    if ((double)f >= (double)dim) /* double holds every u32 exactly */
+        return dim - 1u;
+    return (uint32_t)f;
+}
+
+/* [reorder] §El orden de las celdas: linear index, x varies fastest. */
+static uint32_t linear_cell(uint32_t x, uint32_t y, uint32_t z, uint32_t gx, uint32_t gy)
+{
+    return x + y * gx + z * gx * gy;
+}
+
+/* [count] celdaDe[i] for every particle (parts: N rows of 8 floats). */
+void oracle_cell_index(const float *parts, uint64_t n, const uint32_t dims[3],
+                       const float origin[3], float cellSize, uint32_t *celdaDe)
+{
+    const float invCell = 1.0f / cellSize;
+    for (uint64_t i = 0; i < n; ++i) {
+        const float *pos = parts + ORACLE_FLOATS_PER_PARTICLE * i;
+        uint32_t x = axis_cell(pos[0], origin[0], invCell, dims[0]);
+        uint32_t y = axis_cell(pos[1], origin[1], invCell, dims[1]);
+        uint32_t z = axis_cell(pos[2], origin[2], invCell, dims[2]);
+        celdaDe[i] = linear_cell(x, y, z, dims[0], dims[1]);
+    }
+}
+
+/* [count] §Poner a cero + §El kernel: conteos = histogram of celdaDe. */
+void oracle_histogram(const uint32_t *celdaDe, uint64_t n, uint32_t *conteos, uint64_t cells)
+{
+    memset(conteos, 0, cells * sizeof(uint32_t));
+    for (uint64_t i = 0; i < n; ++i)
+        conteos[celdaDe[i]] += 1u;
+}
+
+/* [scan] inicios[0] = 0, inicios[c+1] = inicios[c] + conteos[c]; C+1 entries. */
+void oracle_exclusive_scan(const uint32_t *conteos, uint64_t cells, uint32_t *inicios)
+{
+    inicios[0] = 0u;
+    for (uint64_t c = 0; c < cells; ++c)
+        inicios[c + 1] = inicios[c] + conteos[c];
+}
+
+/* [scatter] Cursor scatter, particles visited in ascending index (stable). */
+void oracle_scatter(const uint32_t *celdaDe, uint64_t n, const uint32_t *inicios,
+                    uint32_t *cursor, uint64_t cells, uint32_t *ordenado)
+{
+    memset(cursor, 0, cells * sizeof(uint32_t));
+    for (uint64_t i = 0; i < n; ++i) {
+        uint32_t c = celdaDe[i];
+        uint32_t slot = cursor[c];
+        ordenado[inicios[c] + slot] = (uint32_t)i;
+        cursor[c] = slot + 1u;
+    }
+}
+
+/* [reorder] destino[k] = origen[ordenado[k]], whole 32-byte records. */
+void oracle_reorder(const uint32_t *ordenado, uint64_t n, const void *origen, void *destino)
+{
+    const unsigned char *src = (const unsigned char *)origen;
+    unsigned char *dst = (unsigned char *)destino;
+    for (uint64_t k = 0; k < n; ++k)
+        memcpy(dst + ORACLE_RECORD_BYTES * k, src + ORACLE_RECORD_BYTES * (uint64_t)ordenado[k],
+               ORACLE_RECORD_BYTES);
+}
+
+/* The whole chain: cell index, histogram, scan, scatter (stable), gather.
+ * After it conteos holds the histogram again, as it does when the cursor
+ * reuses the counter array and ends at the counts. */
+void oracle_build(const float *origen, uint64_t n, const uint32_t dims[3], const float origin[3],
+                  float cellSize, uint32_t *conteos, uint32_t *celdaDe, uint32_t *inicios,
+                  uint32_t *ordenado, float *destino)
+{
+    const uint64_t cells = (uint64_t)dims[0] * dims[1] * dims[2];
+    oracle_cell_index(origen, n, dims, origin, cellSize, celdaDe);
+    oracle_histogram(celdaDe, n, conteos, cells);
+    oracle_exclusive_scan(conteos, cells, inicios);
+    oracle_scatter(celdaDe, n, inicios, conteos, cells, ordenado);
+    oracle_reorder(ordenado, n, origen, destino);
+}
+
+/* ---- checking helpers (not part of the method) ------------------------- */
+
+static int cmp_u32(const void *a, const void *b)
+{
+    uint32_t x = *(const uint32_t *)a, y = *(const uint32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/* Canonical form of a cell-grouped index array: each segment
+ * [inicios[c], inicios[c+1]) sorted ascending.  Order inside a cell depends
+ * on scheduling ("Construir el índice…", §El orden dentro de la celda), so
+ * results are compared in this form. */
+void oracle_canonicalise(const uint32_t *inicios, uint64_t cells, uint32_t *ordenado)
+{
+    for (uint64_t c = 0; c < cells; ++c) {
+        uint32_t a = inicios[c], b = inicios[c + 1];
+        if (b > a + 1u)
+            qsort(ordenado + a, b - a, sizeof(uint32_t), cmp_u32);
+    }
+}
