@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark of the uniform-grid build on GB300; prints one JSON line.
+
+A step is one whole build (clear, count, scan with the second clear folded
+in, scatter, gather) of the headline scene: 1,000,000 particles uniform in
+[-5, 5)^3 on a 128^3 grid, 32-byte records, inputs resident in HBM.  L2 is
+flushed (a 2 x L2-size buffer is written) between steps, outside the timed
+events.  Per step the build is bracketed by CUDA events on the stream it is
+launched on.
+
+Further passes in the same run:
+  * phase pass   — the same steps through the per-phase entry points, with an
+                   event between phases: per-kernel microseconds and the
+                   roofline of the dominant kernel (the gather);
+  * end to end   — host buffers: pinned host origen -> device, build,
+                   destino and inicios -> pinned host, all inside the events;
+  * cpu baseline — the CPU oracle (single thread) on the same scene.
+
+``--impl reference`` times the CPU oracle alone (the reference arm).
+Under torchrun every rank builds its own replica of the scene ("replicas
+only": the build does not shard); the reported time is the maximum over
+ranks and the value counts every rank's particles.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "grid-build Mparticles/s (count+scan+scatter+gather) at 1M/128³; HBM GB/s"
+UNIT = "Mparticles/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- helpers
+
+def algorithmic_bytes(n: int, cells: int) -> dict:
+    """Minimal bytes each phase must move (every array touched the fewest times
+    the method allows; counter atomics stay in L2 and are not counted)."""
+    return {
+        "clear": 4 * cells,
+        "count": 16 * n + 4 * n,          # pos+vida read, celdaDe write
+        "scan": 4 * cells + 4 * (cells + 1),
+        "clear_cursor": 4 * cells,
+        "scatter": 12 * n,                # celdaDe, inicios[c], ordenado
+        "gather": 68 * n,                 # ordenado, 32-B read, 32-B write
+    }
+
+
+def hbm_peak() -> tuple[float, str]:
+    try:
+        with open(PEAKS_FILE) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(kernel_source: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel (sha256 of the .cu file)."""
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None
+    src = os.path.join(ROOT, "uniform_grid_particle_gb300", "csrc", kernel_source)
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    for line in lines:
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_source:
+            return float(parts[2]) if parts[1] == digest else None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.out.read())) if len(r) >= 9]
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = sorted({name for r in rows for name, v in zip(self.REASONS, r[5:9]) if "Active" in v and "Not" not in v})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    if int(os.environ.get("WORLD_SIZE", "1")) <= 1:
+        return None
+    import torch.distributed as dist
+
+    backend = "nccl" if _cuda_ok() else "gloo"
+    dist.init_process_group(backend)
+    return dist
+
+
+def _cuda_ok() -> bool:
+    import torch
+
+    return torch.cuda.is_available()
+
+
+def max_over_ranks(value: float, dist) -> float:
+    """Largest `value` over all ranks (the job is as slow as its slowest rank)."""
+    if dist is None:
+        return value
+    import torch
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist) -> None:
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_timing(scene, rows, budget_s: float, min_runs: int = 3) -> dict:
+    import oracle
+
+    o = oracle.load()
+    times = []
+    start = time.perf_counter()
+    while len(times) < min_runs or time.perf_counter() - start < budget_s:
+        t0 = time.perf_counter()
+        o.build(rows, scene.dims, scene.origin, scene.cell_size)
+        times.append(time.perf_counter() - t0)
+    per_build = statistics.median(times)
+    return {"value": scene.n / per_build / 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"{len(times)} whole builds of the {scene.name} scene (N={scene.n}, "
+                       f"{scene.dims[0]}^3 cells), single-threaded C oracle, median "
+                       f"{per_build * 1e3:.1f} ms/build; host has {os.cpu_count()} cores")}
+
+
+def run_reference(args) -> None:
+    """The reference arm: the CPU oracle timed on this host's cores.
+
+    Each step is one oracle build with the full grid.  When K + W whole builds
+    would overrun the time budget, each step builds the first n_s particles of
+    the scene instead (n_s chosen from a one-build calibration), and the
+    sample says so."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from uniform_grid_particle_gb300 import scenes
+
+    import oracle
+
+    scene = scenes.SCENES[args.scene]
+    rows = scene.particles()
+    o = oracle.load()
+    t0 = time.perf_counter()
+    o.build(rows, scene.dims, scene.origin, scene.cell_size)
+    t_full = time.perf_counter() - t0
+    per_step = args.reference_budget / (args.steps + args.warmup)
+    n_s = scene.n if t_full <= per_step else max(10_000, int(scene.n * per_step / t_full))
+    sample = rows[:n_s]
+    for _ in range(args.warmup):
+        o.build(sample, scene.dims, scene.origin, scene.cell_size)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        o.build(sample, scene.dims, scene.origin, scene.cell_size)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = n_s / (ms / 1e3) / 1e6
+    what = "whole builds" if n_s == scene.n else f"builds of the first {n_s:,} particles (full grid)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": workload_config(scene, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} {what} of the {scene.name} scene, single-threaded C oracle "
+                                   f"({t_full * 1e3:.1f} ms per whole build); host has {os.cpu_count()} cores"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(scene, args) -> dict:
+    return {
+        "workload": (f"{scene.name}: N={scene.n:,} particles, grid {scene.dims[0]}x{scene.dims[1]}x{scene.dims[2]}"
+                     f" over [-5,5)^3, 32-byte Particula AoS, {scene.kind} positions"),
+        "build": "stable" if args.stable else "atomic cursor",
+        "l2": "flushed between steps (a 2x L2 buffer is written outside the timed events)",
+        "launch": "stream" if not args.graph else "cuda graph",
+    }
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def run_gpu(args) -> None:
+    import numpy as np
+    import torch
+
+    from uniform_grid_particle_gb300 import build as ugbuild
+    from uniform_grid_particle_gb300 import scenes
+
+    dist = dist_setup()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    ugbuild.build()
+    from uniform_grid_particle_gb300 import ugrid as ug
+
+    scene = scenes.SCENES[args.scene]
+    rows = scene.particles()
+    n, cells = scene.n, scene.cells
+    flags = ug.GRID_STABLE if args.stable else 0
+    p = ug.make_params(n, scene.dims, scene.origin, scene.cell_size)
+    b = ug.GridBuffers.allocate(p, flags)
+    origen = torch.from_numpy(rows).cuda()
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device="cuda")
+
+    def step():
+        ug.grid_build(origen, b.destino, b.conteos, b.celdaDe, b.inicios, b.ordenado, b.ws, p, flags, stream)
+
+    graph = None
+    if args.graph:
+        step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        run_step = graph.replay
+    else:
+        run_step = step
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        run_step()
+    torch.cuda.synchronize()
+    if ug.grid_status(b.ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier(dist)
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            flush.fill_(k)
+            starts[k].record(stream)
+            run_step()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if ug.grid_status(b.ws) != 0:
+        raise RuntimeError("device status set during the timed steps")
+    local_total_ms = sum(step_ms)
+    total_ms = max_over_ranks(local_total_ms, dist)
+    ms_per_step = total_ms / args.steps
+    value = world * n / (ms_per_step / 1e3) / 1e6
+    kernels_per_step = 4 + (2 if args.stable else 0)
+
+    # ---- phase pass: per-kernel times, same flushes ----
+    phase_names = ["clear", "count", "scan", "clear_cursor", "scatter", "gather"]
+    phase_ms = {k: [] for k in phase_names}
+    for k in range(args.warmup + args.phase_steps):
+        flush.fill_(k)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        ev[0].record(stream)
+        ug.grid_clear(b.conteos, p, stream)
+        ev[1].record(stream)
+        ug.grid_count(origen, b.conteos, b.celdaDe, p, stream)
+        ev[2].record(stream)
+        ug.grid_scan(b.conteos, b.inicios, b.ws, p, stream)
+        ev[3].record(stream)
+        ug.grid_clear(b.conteos, p, stream)
+        ev[4].record(stream)
+        ug.grid_scatter(b.celdaDe, b.inicios, b.conteos, b.ordenado, b.ws, p, flags, stream)
+        ev[5].record(stream)
+        ug.grid_reorder(b.ordenado, origen, b.destino, b.ws, p, stream)
+        ev[6].record(stream)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            for i, name in enumerate(phase_names):
+                phase_ms[name].append(ev[i].elapsed_time(ev[i + 1]))
+    if ug.grid_status(b.ws) != 0:
+        raise RuntimeError("device status set during the phase pass")
+    phase_us = {k: 1e3 * statistics.mean(v) for k, v in phase_ms.items()}
+    alg = algorithmic_bytes(n, cells)
+    peak, peak_kind = hbm_peak()
+    gather_gbs = alg["gather"] / (phase_us["gather"] * 1e-6) / 1e9
+    traffic = kernel_traffic("reorder.cu")
+
+    # ---- end to end: host buffers, copies inside the events ----
+    host_in = torch.from_numpy(rows).pin_memory()
+    host_dest = torch.empty((n, 8), dtype=torch.float32).pin_memory()
+    host_inicios = torch.empty(cells + 1, dtype=torch.int32).pin_memory()
+    dev_in = torch.empty_like(origen)
+
+    def e2e_step():
+        dev_in.copy_(host_in, non_blocking=True)
+        ug.grid_build(dev_in, b.destino, b.conteos, b.celdaDe, b.inicios, b.ordenado, b.ws, p, flags, stream)
+        host_dest.copy_(b.destino, non_blocking=True)
+        host_inicios.copy_(b.inicios, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for k in range(args.e2e_steps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        e2e_step()
+        e.record(stream)
+        e.synchronize()
+        e2e_ms.append(s.elapsed_time(e))
+    if ug.grid_status(b.ws) != 0:
+        raise RuntimeError("device status set during the end-to-end pass")
+    e2e_total = max_over_ranks(sum(e2e_ms), dist)
+    e2e_value = world * n / (e2e_total / len(e2e_ms) / 1e3) / 1e6
+    if not np.array_equal(host_inicios.numpy()[[0, cells]], np.array([0, n], dtype=np.int32)):
+        raise RuntimeError("end-to-end result is inconsistent")
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    cpu = oracle_timing(scene, rows, args.cpu_budget) if world == 1 else None
+    total_alg = sum(alg.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": workload_config(scene, args),
+        "roofline": {"bound": "hbm", "kernel": "reorder_kernel (gather)", "achieved": gather_gbs,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": gather_gbs / peak,
+                     "traffic": traffic, "algorithmic_bytes": alg["gather"]},
+        "build_hbm": {"algorithmic_bytes": total_alg,
+                      "achieved_gbs": total_alg / (ms_per_step * 1e-3) / 1e9,
+                      "frac_of_nominal_8tbs": total_alg / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
+                      "frac_of_measured": total_alg / (ms_per_step * 1e-3) / 1e9 / peak,
+                      "us_per_build": ms_per_step * 1e3,
+                      "us_min": 1e3 * min(step_ms), "us_median": 1e3 * statistics.median(step_ms)},
+        "phases_us": phase_us,
+        "phases_gbs": {k: alg[k] / (phase_us[k] * 1e-6) / 1e9 for k in phase_names},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(host_in.numel() * 4),
+                "d2h_bytes_per_step": int(host_dest.numel() * 4 + host_inicios.numel() * 4),
+                "ms_per_step": e2e_total / len(e2e_ms)},
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--scene", default="headline")
+    ap.add_argument("--stable", action="store_true", help="time the stable (reproducible) build")
+    ap.add_argument("--graph", action="store_true", help="replay the build from a CUDA graph")
+    ap.add_argument("--phase-steps", type=int, default=500)
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time")
+    ap.add_argument("--reference-budget", type=float, default=150.0,
+                    help="seconds the --impl reference steps may take in all")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

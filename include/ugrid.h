@@ -1,0 +1,181 @@
+/*
+ * ugrid.h — C ABI of libugrid: a uniform spatial grid over particles, built on
+ * one GB300 (sm_103a) as a counting sort keyed by cell index.
+ *
+ * The method is the one of the "guia/webgpu" lessons on blog.wandres.dev:
+ *   "Contar partículas por celda"                       (count, clear)
+ *   "Construir el índice de la rejilla con un prefix sum" (scan, scatter, order)
+ *   "Reordenar por celda y la coalescencia de memoria"   (gather, cell order)
+ *   "El estado de las partículas en storage buffers"     (the 32-byte record)
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers owned by the caller; the library
+ *     allocates no memory and keeps no state between calls (apart from what the
+ *     caller's workspace holds, see grid_workspace_bytes).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream).  Nothing synchronises except grid_status.
+ *   - Return value: GRID_OK when the work was enqueued; GRID_EINVAL (nothing
+ *     enqueued) for a null params pointer, inconsistent params, a null or
+ *     misaligned array, overlapping arrays that must be distinct, unknown flag
+ *     bits; GRID_ECUDA when a CUDA call or launch failed.  Problems the GPU
+ *     finds while running (a look-back wait that timed out, an index out of
+ *     range) are recorded in the workspace status word and returned later by
+ *     grid_status.
+ *   - An empty scene (conteo = 0) is valid; every array of N elements may then
+ *     be NULL.
+ *   - Calls that share a workspace must not overlap on the GPU (use one
+ *     workspace per concurrent stream).
+ */
+#ifndef UGRID_H
+#define UGRID_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The particle record: pos vec3f at byte 0, vida f32 at 12, vel vec3f at 16,
+ * masa f32 at 28; 32 bytes, 16-byte aligned ("El estado de las partículas en
+ * storage buffers", §La estructura y su alineación).  Arrays of it are AoS. */
+typedef struct ugrid_particula {
+    float pos[3];
+    float vida;
+    float vel[3];
+    float masa;
+} ugrid_particula;
+
+/* Grid geometry and sizes.  `conteo` and `celdas` are the Params uniform of
+ * "Contar partículas por celda" (§El kernel); dims/origin/cellSize describe
+ * the grid the cell-index helper uses.
+ *   conteo    N, number of particles (0 allowed).
+ *   celdas    C, number of cells; must equal dims[0]*dims[1]*dims[2] and be
+ *             below 2^32 - 1 (inicios holds C + 1 u32 entries).
+ *   dims      GX, GY, GZ, each >= 1.
+ *   origin    lower corner of cell (0,0,0); finite.
+ *   cellSize  edge of a cubic cell; finite, > 0, with 1.0f/cellSize finite.
+ * Cell of a particle, per axis d (fp32, each operation rounded to nearest, no
+ * fused multiply-add; invCell = 1.0f/cellSize rounded once on the host):
+ *   q_d = clamp(floor((pos_d - origin_d) * invCell), 0, dims_d - 1)
+ * with NaN mapped to 0 and +inf to dims_d - 1; the linear index is
+ *   c = qx + qy*GX + qz*GX*GY
+ * ("Reordenar por celda…", §El orden de las celdas). */
+typedef struct grid_params {
+    uint32_t conteo;
+    uint32_t celdas;
+    uint32_t dims[3];
+    float origin[3];
+    float cellSize;
+} grid_params;
+
+enum grid_status_code {
+    GRID_OK = 0,
+    GRID_EINVAL = 1,   /* bad arguments; nothing was enqueued */
+    GRID_ECUDA = 2,    /* a CUDA call or kernel launch failed */
+    GRID_ETIMEOUT = 3, /* (grid_status) a device-side wait gave up */
+    GRID_EBOUNDS = 4   /* (grid_status) an index read from an input was out of range */
+};
+
+/* flags */
+enum grid_flag {
+    /* Order every cell's particles by ascending particle index after the
+     * scatter, so the result is reproducible bit for bit ("Construir el índice
+     * de la rejilla…", §El orden dentro de la celda: particle index as the
+     * tie-break).  Without it, the order inside a cell depends on scheduling. */
+    GRID_STABLE = 1u
+};
+
+/* Layout of the first 256 bytes of a workspace.  Callers need not touch it;
+ * it is published so that tools and tests can read the status word. */
+typedef struct grid_ws_header {
+    uint32_t status;       /* bit 0: a wait timed out; bit 1: an index was out of range */
+    uint32_t scan_ticket;  /* next tile ticket of the running scan; 0 between calls */
+    uint32_t scan_done;    /* tiles finished by the running scan; 0 between calls */
+    uint32_t stable_big;   /* cells queued for the long-segment sort; 0 between calls */
+    uint32_t stable_done;  /* CTAs finished by the running long-segment sort; 0 between calls */
+    uint32_t reserved[59];
+} grid_ws_header;
+
+/* Bytes of device workspace the calls below need for these params and flags
+ * (the header, the scan's per-tile look-back status words and, with
+ * GRID_STABLE, the segment-sort queue and scratch).  Returns 0 for invalid
+ * params.  The workspace must be 256-byte aligned and zero-filled once after
+ * allocation (grid_workspace_init does that); every call leaves it ready for
+ * the next one.  A workspace sized for one params/flags is valid for any
+ * params with no more cells and particles and a subset of the flags. */
+size_t grid_workspace_bytes(const grid_params *p, unsigned flags);
+
+/* Zero `bytes` of workspace on `stream`. */
+int grid_workspace_init(void *ws, size_t bytes, void *stream);
+
+/* a1 — conteos[0..C) = 0, with cudaMemsetAsync ("Contar partículas por
+ * celda", §Poner a cero dos millones de contadores: a fill done by the copy
+ * path, ordered with the compute work).  conteos: u32[C], 16-byte aligned. */
+int grid_clear(uint32_t *conteos, const grid_params *p, void *stream);
+
+/* a2 — cell index and histogram ("Contar partículas por celda", §El kernel;
+ * §La contención de las celdas densas: particles of one warp that share a cell
+ * add to its counter with one atomic).  For every i < N:
+ *   celdaDe[i] = cell of parts[i].pos;   conteos[celdaDe[i]] += 1.
+ * parts: ugrid_particula[N], 16-byte aligned (read).  conteos: u32[C] (read
+ * and written; the caller zeroes it first, e.g. with grid_clear).
+ * celdaDe: u32[N], 4-byte aligned (written). */
+int grid_count(const ugrid_particula *parts, uint32_t *conteos, uint32_t *celdaDe,
+               const grid_params *p, void *stream);
+
+/* a3 — exclusive scan with the total in an extra slot ("Construir el índice de
+ * la rejilla…", §Del conteo al inicio):
+ *   inicios[0] = 0, inicios[c+1] = inicios[c] + conteos[c], inicios[C] = N.
+ * Single pass with decoupled look-back over tiles of 4096 cells.
+ * conteos: u32[C] (read only).  inicios: u32[C+1] (written).  Both 16-byte
+ * aligned and distinct.  ws: workspace (see grid_workspace_bytes). */
+int grid_scan(const uint32_t *conteos, uint32_t *inicios, void *ws, const grid_params *p,
+              void *stream);
+
+/* a4 — cursor scatter ("Construir el índice de la rejilla…", §La dispersión):
+ * for every i, slot = atomicAdd(&cursor[celdaDe[i]], 1) and
+ * ordenado[inicios[celdaDe[i]] + slot] = i.  Cell c then owns
+ * ordenado[inicios[c] .. inicios[c+1]).  cursor: u32[C], zero on entry (the
+ * pages reuse conteos after a clear); on return it holds the histogram again.
+ * celdaDe: u32[N] and inicios: u32[C+1] (read); ordenado: u32[N] (written).
+ * flags: 0 or GRID_STABLE (then every segment is also sorted ascending).
+ * A cell index >= C or a slot >= N read from the inputs sets status bit 1 and
+ * the write is skipped. */
+int grid_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cursor,
+                 uint32_t *ordenado, unsigned flags, void *ws, const grid_params *p,
+                 void *stream);
+
+/* a5 — gather reorder ("Reordenar por celda y la coalescencia de memoria",
+ * §El kernel de reordenación): destino[k] = origen[ordenado[k]] for k < N,
+ * whole 32-byte records; writes are contiguous, reads scattered.
+ * origen and destino are distinct, non-overlapping ugrid_particula[N] arrays,
+ * 16-byte aligned.  An index >= N sets status bit 1 and that record is not
+ * written. */
+int grid_reorder(const uint32_t *ordenado, const ugrid_particula *origen, ugrid_particula *destino,
+                 void *ws, const grid_params *p, void *stream);
+
+/* The whole build, in the order the pages give ("Construir el índice de la
+ * rejilla…", §La cadena completa): clear conteos, count, scan, clear the
+ * cursor (= conteos), scatter, [segment sort], gather.  The second clear is
+ * folded into the scan, which zeroes each tile of conteos after reading it.
+ * On return (once the stream has run) conteos holds the histogram, celdaDe the
+ * cells, inicios the starts, ordenado the cell-grouped indices and destino
+ * the reordered records.  All seven arrays must be distinct. */
+int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
+               uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, void *ws,
+               unsigned flags, const grid_params *p, void *stream);
+
+/* Synchronise `stream`, read and clear the workspace status word, and return
+ * GRID_OK, GRID_ETIMEOUT (bit 0 set) or GRID_EBOUNDS (bit 1 set); GRID_ECUDA
+ * if the copy or the synchronisation failed. */
+int grid_status(void *ws, void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *grid_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UGRID_H */

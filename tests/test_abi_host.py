@@ -1,0 +1,150 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+sizes its workspace, and rejects bad arguments before any CUDA call."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from uniform_grid_particle_gb300 import build as ugbuild
+
+HEADER = os.path.join(ugbuild.INCLUDE, "ugrid.h")
+EINVAL = 1
+
+
+@pytest.fixture(scope="module")
+def L():
+    ugbuild.build()
+    from uniform_grid_particle_gb300 import ugrid
+
+    return ugrid
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(grid_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 10, names
+    lib = ctypes.CDLL(L.library_path())
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def P(L, n=1000, dims=(16, 16, 16), origin=(-5, -5, -5), cs=0.625):
+    return L.make_params(n, dims, origin, cs)
+
+
+def test_workspace_bytes(L):
+    p = P(L, 1_000_000, (128, 128, 128), cs=0.078125)
+    tiles = (128 ** 3 + 4095) // 4096
+    assert L.grid_workspace_bytes(p, 0) == 256 + ((tiles * 8 + 255) // 256) * 256
+    stable = L.grid_workspace_bytes(p, L.GRID_STABLE)
+    assert stable >= L.grid_workspace_bytes(p, 0) + 4 * 1_000_000
+    assert L.grid_workspace_bytes(p, 2) == 0            # unknown flag
+    bad = P(L)
+    bad.celdas = 7
+    assert L.grid_workspace_bytes(bad, 0) == 0
+    tiny = P(L, 0, (1, 1, 1), cs=1.0)
+    assert L.grid_workspace_bytes(tiny, 0) == 512
+
+
+def test_error_strings(L):
+    for code in range(6):
+        assert L.error_string(code)
+
+
+FAKE = 0x7F0000000000          # 256-aligned, never dereferenced: every call below fails validation
+
+
+def _call(L, name, *args):
+    return getattr(L.lib(), name)(*args)
+
+
+@pytest.mark.parametrize("mutate", [
+    lambda p: setattr(p, "celdas", p.celdas + 1),
+    lambda p: p.dims.__setitem__(0, 0),
+    lambda p: setattr(p, "cellSize", 0.0),
+    lambda p: setattr(p, "cellSize", -1.0),
+    lambda p: setattr(p, "cellSize", math.nan),
+    lambda p: setattr(p, "cellSize", math.inf),
+    lambda p: setattr(p, "cellSize", 1e-45),          # 1/cellSize overflows to inf
+    lambda p: p.origin.__setitem__(1, math.nan),
+    lambda p: p.origin.__setitem__(2, -math.inf),
+], ids=["celdas", "dims0", "cs0", "cs_neg", "cs_nan", "cs_inf", "cs_denorm", "origin_nan", "origin_inf"])
+def test_bad_params_rejected_everywhere(L, mutate):
+    p = P(L)
+    mutate(p)
+    bp = ctypes.byref(p)
+    f = FAKE
+    assert _call(L, "grid_clear", f, bp, None) == EINVAL
+    assert _call(L, "grid_count", f, f + (1 << 30), f + (2 << 30), bp, None) == EINVAL
+    assert _call(L, "grid_scan", f, f + (1 << 30), f + (2 << 30), bp, None) == EINVAL
+    assert _call(L, "grid_scatter", f, f + (1 << 30), f + (2 << 30), f + (3 << 30), 0, f + (4 << 30), bp, None) == EINVAL
+    assert _call(L, "grid_reorder", f, f + (1 << 30), f + (2 << 30), f + (3 << 30), bp, None) == EINVAL
+    assert _call(L, "grid_build", f, f + (1 << 30), f + (2 << 30), f + (3 << 30), f + (4 << 30),
+                 f + (5 << 30), f + (6 << 30), 0, bp, None) == EINVAL
+
+
+def test_cell_count_overflow_rejected(L):
+    p = P(L, 10, (65536, 65536, 1), cs=1.0)     # 2^32 cells: C + 1 would not fit in u32
+    assert L.grid_workspace_bytes(p, 0) == 0
+    p = P(L, 10, (65535, 65537, 1), cs=1.0)     # 2^32 - 1 cells: the largest rejected
+    assert L.grid_workspace_bytes(p, 0) == 0
+    p = P(L, 10, (2, 3, 4), cs=1.0)
+    p.dims[:] = [4294967295, 4294967295, 4294967295]
+    p.celdas = 1
+    assert L.grid_workspace_bytes(p, 0) == 0
+
+
+def test_null_params_and_pointers(L):
+    f = FAKE
+    assert _call(L, "grid_clear", f, None, None) == EINVAL
+    assert L.lib().grid_workspace_bytes(None, 0) == 0
+    p = P(L)
+    bp = ctypes.byref(p)
+    assert _call(L, "grid_clear", None, bp, None) == EINVAL
+    assert _call(L, "grid_count", None, f, f + (1 << 30), bp, None) == EINVAL
+    assert _call(L, "grid_reorder", f, f + (1 << 30), f + (2 << 30), None, bp, None) == EINVAL
+    assert _call(L, "grid_status", None, None) == EINVAL
+    assert _call(L, "grid_workspace_init", None, 4096, None) == EINVAL
+
+
+def test_alignment_rules(L):
+    p = P(L)
+    bp = ctypes.byref(p)
+    f = FAKE
+    # particles must be 16-byte aligned, conteos 16, celdaDe 4
+    assert _call(L, "grid_count", f + 8, f + (1 << 30), f + (2 << 30), bp, None) == EINVAL
+    assert _call(L, "grid_count", f, f + (1 << 30) + 4, f + (2 << 30), bp, None) == EINVAL
+    assert _call(L, "grid_count", f, f + (1 << 30), f + (2 << 30) + 2, bp, None) == EINVAL
+    # the workspace must be 256-byte aligned
+    assert _call(L, "grid_scan", f, f + (1 << 30), f + (2 << 30) + 16, bp, None) == EINVAL
+    assert _call(L, "grid_workspace_init", f + 16, 4096, None) == EINVAL
+
+
+def test_overlapping_buffers_rejected(L):
+    p = P(L, 1000)
+    bp = ctypes.byref(p)
+    f = FAKE
+    # destino overlapping origen (in-place gather is refused)
+    assert _call(L, "grid_reorder", f + (3 << 30), f, f + 1024, f + (4 << 30), bp, None) == EINVAL
+    assert _call(L, "grid_reorder", f + (3 << 30), f, f, f + (4 << 30), bp, None) == EINVAL
+    # inicios overlapping conteos in the scan
+    assert _call(L, "grid_scan", f, f + 4096, f + (2 << 30), bp, None) == EINVAL
+    # cursor aliasing celdaDe in the scatter
+    assert _call(L, "grid_scatter", f, f + (1 << 30), f, f + (3 << 30), 0, f + (4 << 30), bp, None) == EINVAL
+    # unknown flag bits
+    assert _call(L, "grid_scatter", f, f + (1 << 30), f + (2 << 30), f + (3 << 30), 4, f + (4 << 30), bp, None) == EINVAL
+
+
+def test_binding_checks_tensors_before_the_library(L):
+    import torch
+
+    p = P(L, 10)
+    with pytest.raises(ValueError):
+        L.grid_clear(torch.zeros(4096, dtype=torch.int32), p)          # CPU tensor

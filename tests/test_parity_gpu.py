@@ -1,0 +1,170 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_matches_oracle, gpu_build, special_rows, to_u32
+from uniform_grid_particle_gb300 import scenes
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ug():
+    from uniform_grid_particle_gb300 import build, ugrid
+
+    build.build()
+    assert torch.cuda.is_available()
+    return ugrid
+
+
+def _check(ug, o, rows, dims, origin, cs, stable):
+    flags = ug.GRID_STABLE if stable else 0
+    got = gpu_build(ug, rows, dims, origin, cs, flags)
+    ref = o.build(rows, dims, origin, cs)
+    assert_matches_oracle(o, rows, got, ref, stable)
+    return got
+
+
+# ---------------------------------------------------------------- the workloads
+
+@pytest.mark.parametrize("stable", [False, True], ids=["atomic", "stable"])
+@pytest.mark.parametrize("name", ["tiny", "scan_dominated", "headline", "contention", "stress"])
+def test_scene_build(ug, oracle_lib, name, stable):
+    s = scenes.SCENES[name]
+    rows = s.particles()
+    _check(ug, oracle_lib, rows, s.dims, s.origin, s.cell_size, stable)
+
+
+def test_contention_unshuffled(ug, oracle_lib):
+    rows = scenes.contention_particles(1_000_000, 99, 128, shuffle=False)
+    _check(ug, oracle_lib, rows, (128,) * 3, (-5.0,) * 3, 0.078125, False)
+    _check(ug, oracle_lib, rows, (128,) * 3, (-5.0,) * 3, 0.078125, True)
+
+
+# ---------------------------------------------------------------- ragged shapes
+
+RAGGED = [(1, (17, 19, 23)), (33, (17, 19, 23)), (1023, (5, 3, 2)), (1025, (17, 19, 23)),
+          (4096 * 3 + 77, (17, 19, 23)), (100_003, (31, 7, 61)), (65_537, (1, 1, 1)),
+          (250_000, (64, 1, 9))]
+
+
+@pytest.mark.parametrize("stable", [False, True], ids=["atomic", "stable"])
+@pytest.mark.parametrize("n,dims", RAGGED, ids=[f"{n}-{d[0]}x{d[1]}x{d[2]}" for n, d in RAGGED])
+def test_ragged(ug, oracle_lib, n, dims, stable):
+    origin = (np.float32(-1.3), np.float32(2.2), np.float32(0.7))
+    cs = np.float32(0.37)
+    rng = np.random.default_rng(n)
+    lo = np.array(origin, np.float64) - 0.5
+    hi = np.array(origin, np.float64) + np.array(dims) * float(cs) + 0.5
+    rows = np.zeros((n, 8), np.float32)
+    rows[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+    rows[:, 3:] = rng.random((n, 5)).astype(np.float32)
+    _check(ug, oracle_lib, rows, dims, origin, cs, stable)
+
+
+# ---------------------------------------------------------------- cell-index edge cases
+
+@pytest.mark.parametrize("dims,cs", [((16,) * 3, 0.625), ((128,) * 3, 0.078125), ((256,) * 3, 0.0390625),
+                                     ((37, 11, 5), 0.1), ((9, 40, 13), 0.3)])
+def test_faces_ulps_and_specials(ug, oracle_lib, dims, cs):
+    origin = (np.float32(-5.0), np.float32(-1.7), np.float32(3.3))
+    rows = special_rows(dims, origin, np.float32(cs), seed=dims[0])
+    _check(ug, oracle_lib, rows, dims, origin, np.float32(cs), False)
+
+
+# ---------------------------------------------------------------- degenerate cases
+
+def test_empty_scene(ug, oracle_lib):
+    rows = np.zeros((0, 8), np.float32)
+    got = gpu_build(ug, rows, (8, 8, 8), (0, 0, 0), 1.0)
+    assert got["status"] == 0
+    assert not got["conteos"].any() and not got["inicios"].any() and got["inicios"].size == 513
+
+
+def test_single_cell_grid(ug, oracle_lib):
+    rows = scenes.uniform_particles(70_001, 3)
+    _check(ug, oracle_lib, rows, (1, 1, 1), (-5, -5, -5), 10.0, False)
+    _check(ug, oracle_lib, rows, (1, 1, 1), (-5, -5, -5), 10.0, True)
+
+
+@pytest.mark.parametrize("n", [2, 33, 10_000, 16_384, 16_385, 1_000_000])
+def test_all_particles_in_one_cell(ug, oracle_lib, n):
+    """Every particle on one cell centre: maximal contention, one long segment
+    (register, shared-memory and radix tiers of the stable sort)."""
+    rows = scenes.single_cell_particles(n, 5, (0.0390625,) * 3)
+    got = _check(ug, oracle_lib, rows, (128,) * 3, (-5.0,) * 3, 0.078125, True)
+    assert np.array_equal(got["ordenado"], np.arange(n, dtype=np.uint32))
+    _check(ug, oracle_lib, rows, (128,) * 3, (-5.0,) * 3, 0.078125, False)
+
+
+def test_large_grid(ug, oracle_lib):
+    """512^3 cells: 32768 scan tiles in one look-back chain."""
+    rows = scenes.uniform_particles(2_000_000, 17)
+    _check(ug, oracle_lib, rows, (512,) * 3, (-5.0,) * 3, np.float32(10 / 512), False)
+
+
+def test_stable_mode_is_deterministic(ug, oracle_lib):
+    s = scenes.SCENES["contention"]
+    rows = s.particles()
+    a = gpu_build(ug, rows, s.dims, s.origin, s.cell_size, ug.GRID_STABLE)
+    b = gpu_build(ug, rows, s.dims, s.origin, s.cell_size, ug.GRID_STABLE)
+    assert np.array_equal(a["ordenado"], b["ordenado"])
+    assert np.array_equal(a["destino"].view(np.uint32), b["destino"].view(np.uint32))
+
+
+# ---------------------------------------------------------------- one entry point at a time
+
+def test_phases_one_by_one(ug, oracle_lib):
+    o = oracle_lib
+    s = scenes.SCENES["headline"]
+    rows = s.particles()
+    n, dims, C = s.n, s.dims, s.cells
+    p = ug.make_params(n, dims, s.origin, s.cell_size)
+    ref = o.build(rows, dims, s.origin, s.cell_size)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).cuda()  # noqa: E731
+    origen = torch.from_numpy(rows).cuda()
+    ws = torch.zeros(ug.grid_workspace_bytes(p, ug.GRID_STABLE), dtype=torch.uint8, device="cuda")
+
+    conteos = torch.full((C,), 7, dtype=torch.int32, device="cuda")
+    celda = torch.empty(n, dtype=torch.int32, device="cuda")
+    ug.grid_clear(conteos, p)
+    assert not conteos.any()
+    ug.grid_count(origen, conteos, celda, p)
+    assert np.array_equal(to_u32(celda), ref["celdaDe"])
+    assert np.array_equal(to_u32(conteos), ref["conteos"])
+
+    inicios = torch.empty(C + 1, dtype=torch.int32, device="cuda")
+    ug.grid_scan(dev(ref["conteos"]), inicios, ws, p)
+    assert np.array_equal(to_u32(inicios), ref["inicios"])
+
+    cursor = torch.zeros(C, dtype=torch.int32, device="cuda")
+    ordenado = torch.empty(n, dtype=torch.int32, device="cuda")
+    ug.grid_scatter(dev(ref["celdaDe"]), dev(ref["inicios"]), cursor, ordenado, ws, p)
+    assert ug.grid_status(ws) == 0
+    assert np.array_equal(to_u32(cursor), ref["conteos"]), "cursor ends at the histogram"
+    assert np.array_equal(o.canonicalise(ref["inicios"], to_u32(ordenado)), ref["ordenado"])
+
+    cursor.zero_()
+    ug.grid_scatter(dev(ref["celdaDe"]), dev(ref["inicios"]), cursor, ordenado, ws, p, flags=ug.GRID_STABLE)
+    assert ug.grid_status(ws) == 0
+    assert np.array_equal(to_u32(ordenado), ref["ordenado"])
+
+    destino = torch.empty_like(origen)
+    ug.grid_reorder(dev(ref["ordenado"]), origen, destino, ws, p)
+    assert ug.grid_status(ws) == 0
+    assert np.array_equal(destino.cpu().numpy().view(np.uint32), ref["destino"].view(np.uint32))
+
+
+def test_scan_large_counts(ug, oracle_lib):
+    """Counts up to 1000 per cell (totals near 2^31) over a ragged cell count."""
+    C = 2_097_152 + 1234
+    rng = np.random.default_rng(4)
+    conteos = rng.integers(0, 1000, C, dtype=np.uint32)
+    p = ug.make_params(int(conteos.sum()) & 0xFFFFFFFF, (C, 1, 1), (0, 0, 0), 1.0)
+    ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
+    inicios = torch.empty(C + 1, dtype=torch.int32, device="cuda")
+    for _ in range(3):   # the workspace is reusable call after call
+        ug.grid_scan(torch.from_numpy(conteos.view(np.int32)).cuda(), inicios, ws, p)
+        assert np.array_equal(to_u32(inicios), oracle_lib.exclusive_scan(conteos))
+    assert ug.grid_status(ws) == 0

@@ -1,0 +1,243 @@
+// C ABI of libugrid: argument checks, workspace layout and the launch order.
+// Every check runs before the first CUDA call, so a rejected call enqueues
+// nothing (and works on a machine without a GPU).
+#include <cmath>
+#include <cstring>
+
+#include "ugrid_internal.cuh"
+
+namespace ugrid {
+
+static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+WsLayout ws_layout(uint64_t n, uint64_t cells, unsigned flags) {
+    WsLayout l{};
+    size_t off = kHeaderBytes;
+    l.tile_status = off;
+    off = round_up(off + scan_tiles(cells) * sizeof(unsigned long long), 256);
+    if (flags & GRID_STABLE) {
+        l.stable_queue = off;
+        off = round_up(off + segment_queue_capacity(n, cells) * sizeof(uint32_t), 256);
+        l.stable_scratch = off;
+        off = round_up(off + n * sizeof(uint32_t), 256);
+    }
+    l.total = off;
+    return l;
+}
+
+}  // namespace ugrid
+
+using namespace ugrid;
+
+namespace {
+
+constexpr uint64_t kMaxCells = 0xfffffffeull;  // C + 1 must fit in u32
+
+bool check_params(const grid_params *p, Geometry *g) {
+    if (p == nullptr) return false;
+    uint64_t c = 1;
+    for (int d = 0; d < 3; ++d) {
+        if (p->dims[d] == 0) return false;
+        c *= p->dims[d];
+        if (c > kMaxCells) return false;
+    }
+    if (c != p->celdas) return false;
+    for (int d = 0; d < 3; ++d)
+        if (!std::isfinite(p->origin[d])) return false;
+    if (!std::isfinite(p->cellSize) || !(p->cellSize > 0.0f)) return false;
+    const float inv = 1.0f / p->cellSize;  // fp32, rounded to nearest, once
+    if (!std::isfinite(inv)) return false;
+    if (g != nullptr) {
+        for (int d = 0; d < 3; ++d) {
+            g->origin[d] = p->origin[d];
+            g->dims[d] = p->dims[d];
+        }
+        g->inv_cell = inv;
+    }
+    return true;
+}
+
+// An array of `count` elements: may be NULL only when empty; aligned otherwise.
+bool array_ok(const void *ptr, uint64_t count, size_t align) {
+    if (count == 0) return true;
+    return ptr != nullptr && reinterpret_cast<uintptr_t>(ptr) % align == 0;
+}
+
+struct Span {
+    const void *ptr;
+    uint64_t bytes;
+};
+
+bool disjoint(const Span *s, int k) {
+    for (int a = 0; a < k; ++a)
+        for (int b = a + 1; b < k; ++b) {
+            if (s[a].bytes == 0 || s[b].bytes == 0) continue;
+            const uintptr_t pa = reinterpret_cast<uintptr_t>(s[a].ptr);
+            const uintptr_t pb = reinterpret_cast<uintptr_t>(s[b].ptr);
+            if (pa < pb + s[b].bytes && pb < pa + s[a].bytes) return false;
+        }
+    return true;
+}
+
+int cuda_code(cudaError_t e) { return e == cudaSuccess ? GRID_OK : GRID_ECUDA; }
+
+grid_ws_header *header(void *ws) { return static_cast<grid_ws_header *>(ws); }
+
+unsigned long long *tile_status(void *ws, const WsLayout &l) {
+    return reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + l.tile_status);
+}
+
+constexpr size_t kRecord = sizeof(ugrid_particula);
+static_assert(sizeof(ugrid_particula) == 32, "Particula is 32 bytes");
+static_assert(offsetof(ugrid_particula, vida) == 12, "vida at byte 12");
+static_assert(offsetof(ugrid_particula, vel) == 16, "vel at byte 16");
+static_assert(offsetof(ugrid_particula, masa) == 28, "masa at byte 28");
+static_assert(sizeof(grid_ws_header) == kHeaderBytes, "workspace header is 256 bytes");
+
+}  // namespace
+
+extern "C" {
+
+size_t grid_workspace_bytes(const grid_params *p, unsigned flags) {
+    if (!check_params(p, nullptr) || (flags & ~GRID_STABLE)) return 0;
+    return ws_layout(p->conteo, p->celdas, flags).total;
+}
+
+int grid_workspace_init(void *ws, size_t bytes, void *stream) {
+    if (ws == nullptr || bytes < kHeaderBytes || reinterpret_cast<uintptr_t>(ws) % 256) return GRID_EINVAL;
+    return cuda_code(cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream)));
+}
+
+int grid_clear(uint32_t *conteos, const grid_params *p, void *stream) {
+    if (!check_params(p, nullptr) || !array_ok(conteos, p->celdas, 16)) return GRID_EINVAL;
+    return cuda_code(cudaMemsetAsync(conteos, 0, (size_t)p->celdas * sizeof(uint32_t),
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int grid_count(const ugrid_particula *parts, uint32_t *conteos, uint32_t *celdaDe,
+               const grid_params *p, void *stream) {
+    Geometry g;
+    if (!check_params(p, &g)) return GRID_EINVAL;
+    const uint64_t n = p->conteo, c = p->celdas;
+    if (!array_ok(parts, n, 16) || !array_ok(conteos, c, 16) || !array_ok(celdaDe, n, 4))
+        return GRID_EINVAL;
+    const Span s[] = {{parts, n * kRecord}, {conteos, c * 4}, {celdaDe, n * 4}};
+    if (!disjoint(s, 3)) return GRID_EINVAL;
+    return cuda_code(launch_count(parts, conteos, celdaDe, p->conteo, g,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int grid_scan(const uint32_t *conteos, uint32_t *inicios, void *ws, const grid_params *p,
+              void *stream) {
+    if (!check_params(p, nullptr)) return GRID_EINVAL;
+    const uint64_t c = p->celdas;
+    const WsLayout l = ws_layout(p->conteo, c, 0);
+    if (!array_ok(conteos, c, 16) || !array_ok(inicios, c + 1, 16) || !array_ok(ws, l.total, 256))
+        return GRID_EINVAL;
+    const Span s[] = {{conteos, c * 4}, {inicios, (c + 1) * 4}, {ws, l.total}};
+    if (!disjoint(s, 3)) return GRID_EINVAL;
+    return cuda_code(launch_scan(const_cast<uint32_t *>(conteos), inicios, c, false, header(ws),
+                                 tile_status(ws, l), static_cast<cudaStream_t>(stream)));
+}
+
+int grid_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cursor,
+                 uint32_t *ordenado, unsigned flags, void *ws, const grid_params *p,
+                 void *stream) {
+    if (!check_params(p, nullptr) || (flags & ~GRID_STABLE)) return GRID_EINVAL;
+    const uint64_t n = p->conteo, c = p->celdas;
+    const WsLayout l = ws_layout(n, c, flags);
+    if (!array_ok(celdaDe, n, 4) || !array_ok(inicios, c + 1, 4) || !array_ok(cursor, c, 4) ||
+        !array_ok(ordenado, n, 4) || !array_ok(ws, l.total, 256))
+        return GRID_EINVAL;
+    const Span s[] = {{celdaDe, n * 4}, {inicios, (c + 1) * 4}, {cursor, c * 4},
+                      {ordenado, n * 4}, {ws, l.total}};
+    if (!disjoint(s, 5)) return GRID_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    grid_ws_header *h = header(ws);
+    cudaError_t e = launch_scatter(celdaDe, inicios, cursor, ordenado, p->conteo, p->celdas,
+                                   &h->status, st);
+    if (e == cudaSuccess && (flags & GRID_STABLE)) {
+        char *base = static_cast<char *>(ws);
+        e = launch_segment_sort(inicios, ordenado, p->conteo, p->celdas, h,
+                                reinterpret_cast<uint32_t *>(base + l.stable_queue),
+                                reinterpret_cast<uint32_t *>(base + l.stable_scratch), st);
+    }
+    return cuda_code(e);
+}
+
+int grid_reorder(const uint32_t *ordenado, const ugrid_particula *origen, ugrid_particula *destino,
+                 void *ws, const grid_params *p, void *stream) {
+    if (!check_params(p, nullptr)) return GRID_EINVAL;
+    const uint64_t n = p->conteo;
+    if (!array_ok(ordenado, n, 4) || !array_ok(origen, n, 16) || !array_ok(destino, n, 16) ||
+        !array_ok(ws, kHeaderBytes, 256))
+        return GRID_EINVAL;
+    const Span s[] = {{ordenado, n * 4}, {origen, n * kRecord}, {destino, n * kRecord},
+                      {ws, kHeaderBytes}};
+    if (!disjoint(s, 4)) return GRID_EINVAL;
+    return cuda_code(launch_reorder(ordenado, origen, destino, p->conteo, &header(ws)->status,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
+               uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, void *ws,
+               unsigned flags, const grid_params *p, void *stream) {
+    Geometry g;
+    if (!check_params(p, &g) || (flags & ~GRID_STABLE)) return GRID_EINVAL;
+    const uint64_t n = p->conteo, c = p->celdas;
+    const WsLayout l = ws_layout(n, c, flags);
+    if (!array_ok(origen, n, 16) || !array_ok(destino, n, 16) || !array_ok(conteos, c, 16) ||
+        !array_ok(celdaDe, n, 4) || !array_ok(inicios, c + 1, 16) || !array_ok(ordenado, n, 4) ||
+        !array_ok(ws, l.total, 256))
+        return GRID_EINVAL;
+    const Span s[] = {{origen, n * kRecord}, {destino, n * kRecord}, {conteos, c * 4},
+                      {celdaDe, n * 4},      {inicios, (c + 1) * 4}, {ordenado, n * 4},
+                      {ws, l.total}};
+    if (!disjoint(s, 7)) return GRID_EINVAL;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    grid_ws_header *h = header(ws);
+    cudaError_t e = cudaMemsetAsync(conteos, 0, c * sizeof(uint32_t), st);  // a1
+    if (e == cudaSuccess) e = launch_count(origen, conteos, celdaDe, p->conteo, g, st);  // a2
+    if (e == cudaSuccess)  // a3 and a1' (conteos zeroed tile by tile for reuse as the cursor)
+        e = launch_scan(conteos, inicios, c, true, h, tile_status(ws, l), st);
+    if (e == cudaSuccess)  // a4
+        e = launch_scatter(celdaDe, inicios, conteos, ordenado, p->conteo, p->celdas, &h->status, st);
+    if (e == cudaSuccess && (flags & GRID_STABLE)) {  // a6
+        char *base = static_cast<char *>(ws);
+        e = launch_segment_sort(inicios, ordenado, p->conteo, p->celdas, h,
+                                reinterpret_cast<uint32_t *>(base + l.stable_queue),
+                                reinterpret_cast<uint32_t *>(base + l.stable_scratch), st);
+    }
+    if (e == cudaSuccess) e = launch_reorder(ordenado, origen, destino, p->conteo, &h->status, st);  // a5
+    return cuda_code(e);
+}
+
+int grid_status(void *ws, void *stream) {
+    if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256) return GRID_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return GRID_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GRID_ECUDA;
+    if (word != 0) {
+        if (cudaMemsetAsync(ws, 0, sizeof(word), st) != cudaSuccess) return GRID_ECUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return GRID_ECUDA;
+    }
+    if (word & kStatusTimeout) return GRID_ETIMEOUT;
+    if (word & kStatusBounds) return GRID_EBOUNDS;
+    return GRID_OK;
+}
+
+const char *grid_error_string(int code) {
+    switch (code) {
+        case GRID_OK: return "ok";
+        case GRID_EINVAL: return "invalid argument (nothing was enqueued)";
+        case GRID_ECUDA: return "a CUDA call or kernel launch failed";
+        case GRID_ETIMEOUT: return "a device-side wait timed out";
+        case GRID_EBOUNDS: return "an index read from an input was out of range";
+        default: return "unknown status code";
+    }
+}
+
+}  // extern "C"
