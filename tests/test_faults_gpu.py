@@ -26,8 +26,8 @@ def ug():
 
 
 def test_lookback_wait_times_out_and_workspace_recovers(ug, oracle_lib):
-    dims = (32, 32, 16)                      # 16384 cells = 4 scan tiles
-    C = 32 * 32 * 16
+    dims = (64, 64, 16)                      # 65536 cells = 8 scan tiles
+    C = 64 * 64 * 16
     rng = np.random.default_rng(1)
     conteos = rng.integers(0, 5, C, dtype=np.uint32)
     p = ug.make_params(int(conteos.sum()), dims, (0, 0, 0), 1.0)

@@ -15,6 +15,10 @@ WsLayout ws_layout(uint64_t n, uint64_t cells, unsigned flags) {
     size_t off = kHeaderBytes;
     l.tile_status = off;
     off = round_up(off + scan_tiles(cells) * sizeof(unsigned long long), 256);
+    l.chunk_sums = off;
+    off = round_up(off + kFusedMaxCtas * sizeof(uint32_t), 256);
+    l.slots = off;
+    off = round_up(off + n * sizeof(uint32_t), 256);
     if (flags & GRID_STABLE) {
         l.stable_queue = off;
         off = round_up(off + segment_queue_capacity(n, cells) * sizeof(uint32_t), 256);
@@ -123,8 +127,9 @@ int grid_count(const ugrid_particula *parts, uint32_t *conteos, uint32_t *celdaD
         return GRID_EINVAL;
     const Span s[] = {{parts, n * kRecord}, {conteos, c * 4}, {celdaDe, n * 4}};
     if (!disjoint(s, 3)) return GRID_EINVAL;
+    // Launched normally: it usually follows the clear (a memset).
     return cuda_code(launch_count(parts, conteos, celdaDe, p->conteo, g,
-                                  static_cast<cudaStream_t>(stream)));
+                                  static_cast<cudaStream_t>(stream), false));
 }
 
 int grid_scan(const uint32_t *conteos, uint32_t *inicios, void *ws, const grid_params *p,
@@ -137,7 +142,7 @@ int grid_scan(const uint32_t *conteos, uint32_t *inicios, void *ws, const grid_p
     const Span s[] = {{conteos, c * 4}, {inicios, (c + 1) * 4}, {ws, l.total}};
     if (!disjoint(s, 3)) return GRID_EINVAL;
     return cuda_code(launch_scan(const_cast<uint32_t *>(conteos), inicios, c, false, header(ws),
-                                 tile_status(ws, l), static_cast<cudaStream_t>(stream)));
+                                 tile_status(ws, l), static_cast<cudaStream_t>(stream), true));
 }
 
 int grid_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cursor,
@@ -155,12 +160,12 @@ int grid_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cur
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     grid_ws_header *h = header(ws);
     cudaError_t e = launch_scatter(celdaDe, inicios, cursor, ordenado, p->conteo, p->celdas,
-                                   &h->status, st);
+                                   &h->status, st, true);
     if (e == cudaSuccess && (flags & GRID_STABLE)) {
         char *base = static_cast<char *>(ws);
         e = launch_segment_sort(inicios, ordenado, p->conteo, p->celdas, h,
                                 reinterpret_cast<uint32_t *>(base + l.stable_queue),
-                                reinterpret_cast<uint32_t *>(base + l.stable_scratch), st);
+                                reinterpret_cast<uint32_t *>(base + l.stable_scratch), st, true);
     }
     return cuda_code(e);
 }
@@ -176,7 +181,7 @@ int grid_reorder(const uint32_t *ordenado, const ugrid_particula *origen, ugrid_
                       {ws, kHeaderBytes}};
     if (!disjoint(s, 4)) return GRID_EINVAL;
     return cuda_code(launch_reorder(ordenado, origen, destino, p->conteo, &header(ws)->status,
-                                    static_cast<cudaStream_t>(stream)));
+                                    static_cast<cudaStream_t>(stream), true));
 }
 
 int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
@@ -197,19 +202,32 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     grid_ws_header *h = header(ws);
+    char *base = static_cast<char *>(ws);
+    if (!(flags & GRID_STABLE)) {
+        // The whole chain in one cooperative launch (build_fused.cu).
+        const cudaError_t f = launch_build_fused(
+            origen, destino, conteos, celdaDe, inicios, ordenado, p->conteo, c, g, h,
+            reinterpret_cast<uint32_t *>(base + l.chunk_sums),
+            reinterpret_cast<uint32_t *>(base + l.slots), st);
+        if (f != cudaErrorNotSupported) return cuda_code(f);
+        (void)cudaGetLastError();  // not supported here: one launch per phase instead
+    }
     cudaError_t e = cudaMemsetAsync(conteos, 0, c * sizeof(uint32_t), st);  // a1
-    if (e == cudaSuccess) e = launch_count(origen, conteos, celdaDe, p->conteo, g, st);  // a2
+    // After the memset the kernels follow one another with programmatic
+    // dependent launch: each may start while the previous one drains.
+    if (e == cudaSuccess) e = launch_count(origen, conteos, celdaDe, p->conteo, g, st, false);  // a2
     if (e == cudaSuccess)  // a3 and a1' (conteos zeroed tile by tile for reuse as the cursor)
-        e = launch_scan(conteos, inicios, c, true, h, tile_status(ws, l), st);
+        e = launch_scan(conteos, inicios, c, true, h, tile_status(ws, l), st, true);
     if (e == cudaSuccess)  // a4
-        e = launch_scatter(celdaDe, inicios, conteos, ordenado, p->conteo, p->celdas, &h->status, st);
+        e = launch_scatter(celdaDe, inicios, conteos, ordenado, p->conteo, p->celdas, &h->status,
+                           st, true);
     if (e == cudaSuccess && (flags & GRID_STABLE)) {  // a6
-        char *base = static_cast<char *>(ws);
         e = launch_segment_sort(inicios, ordenado, p->conteo, p->celdas, h,
                                 reinterpret_cast<uint32_t *>(base + l.stable_queue),
-                                reinterpret_cast<uint32_t *>(base + l.stable_scratch), st);
+                                reinterpret_cast<uint32_t *>(base + l.stable_scratch), st, true);
     }
-    if (e == cudaSuccess) e = launch_reorder(ordenado, origen, destino, p->conteo, &h->status, st);  // a5
+    if (e == cudaSuccess)  // a5
+        e = launch_reorder(ordenado, origen, destino, p->conteo, &h->status, st, true);
     return cuda_code(e);
 }
 

@@ -1,0 +1,422 @@
+// The whole (non-stable) grid build in one cooperative launch.
+//
+// The pages chain separate dispatches because the phases depend on each other
+// across workgroups ("Construir el índice de la rejilla…", §La cadena
+// completa: the scan needs every count, the scatter every start).  Here every
+// CTA of the grid is resident at once (cooperative launch, one or two CTAs
+// per SM), so a grid-wide barrier stands in for each kernel boundary:
+//
+//   clear   conteos[0..C) = 0                              ("Poner a cero")
+//   count   celdaDe[i] = cell of particle i; the atomic that counts it
+//           returns its slot in the cell, kept in slots[i]  ("El kernel";
+//           the counter array is the cursor of "La dispersión")
+//   scan a  each CTA totals one contiguous chunk of conteos
+//   scan b  each CTA adds the totals of the chunks before it and scans its
+//           chunk into inicios; the last CTA writes inicios[C] = N
+//                                                     ("Del conteo al inicio")
+//   scatter ordenado[inicios[c] + slots[i]] = i        ("La dispersión")
+//   gather  destino[k] = origen[ordenado[k]]   ("El kernel de reordenación")
+//
+// Because the count's atomic already hands out the slot, the pages' second
+// clear and second atomic pass are not needed: conteos ends as the histogram,
+// exactly as after their cursor scatter, and every output is one the pages'
+// chain can produce (order inside a cell is the atomics' arrival order).
+//
+// The count reads each record's first 16 bytes with an L2 evict-last policy
+// and the gather reads the records with evict-first: the 32-byte sectors the
+// count brings into L2 are still there when the gather needs them.
+//
+// Grid barriers: every CTA adds one to a counter; the last one resets the
+// counter and bumps a generation word that the others poll with acquire
+// loads.  A wait gives up after kSpinLimitNs and records kStatusTimeout, so
+// the kernel cannot hang (co-residency is guaranteed by the cooperative
+// launch, so the limit is a guard, not part of the protocol).
+#include <atomic>
+
+#include "ugrid_internal.cuh"
+
+namespace ugrid {
+namespace {
+
+// Measurement hook at each phase boundary; compiled out unless a profiling
+// build defines it.
+#ifndef UGRID_PHASE_MARK
+#define UGRID_PHASE_MARK(phase)
+#endif
+#ifndef UGRID_PHASE_END
+#define UGRID_PHASE_END(phase)
+#endif
+
+#ifndef UGRID_FUSED_COUNT_ITEMS
+#define UGRID_FUSED_COUNT_ITEMS 4
+#endif
+#ifndef UGRID_FUSED_SCATTER_ITEMS
+#define UGRID_FUSED_SCATTER_ITEMS 8
+#endif
+#ifndef UGRID_FUSED_GATHER_ITEMS
+#define UGRID_FUSED_GATHER_ITEMS 4
+#endif
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCountItems = UGRID_FUSED_COUNT_ITEMS;      // particles per thread per round
+constexpr int kScatterItems = UGRID_FUSED_SCATTER_ITEMS;  // particles per thread per round
+constexpr int kGatherItems = UGRID_FUSED_GATHER_ITEMS;    // half-records per thread per round
+constexpr int kScanVecs = 4;  // 16-byte vectors of counts a thread keeps between the scan phases
+constexpr int kMaxDevices = 64;
+
+__device__ __forceinline__ uint32_t load_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void store_release(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint4 load_policy(const uint4 *p, unsigned long long policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t *p) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
+}
+
+// Thread 0 of every CTA carries `gen`, the barrier generation it waits past.
+// Arrival is a release (acq_rel) add, so the CTA's writes — made visible to
+// thread 0 by the __syncthreads — are published with it; the last CTA to
+// arrive has acquired every other arrival through the chain of adds, resets
+// the counter and publishes the new generation with a release store, which
+// the others read with acquire loads.
+__device__ void grid_barrier(grid_ws_header *hdr, uint32_t &gen) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t target = gen + 1u;
+        if (arrive_acq_rel(&hdr->bar_count) == gridDim.x - 1u) {
+            hdr->bar_count = 0u;
+            store_release(&hdr->bar_gen, target);
+        } else {
+            const unsigned long long start = global_ns();
+            while (load_acquire(&hdr->bar_gen) != target) {
+                __nanosleep(20);
+                if (global_ns() - start > kSpinLimitNs) {
+                    record_status(&hdr->status, kStatusTimeout);
+                    break;
+                }
+            }
+        }
+        gen = target;
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v) {
+    const uint32_t lane = lane_id();
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= (uint32_t)o) v += t;
+    }
+    return v;
+}
+
+// Block-wide sum (every thread gets it).
+__device__ uint32_t block_sum(uint32_t v, uint32_t *s_red) {
+    v = __reduce_add_sync(0xffffffffu, v);
+    if (lane_id() == 0) s_red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += s_red[w];
+    __syncthreads();
+    return t;
+}
+
+// Block-wide exclusive scan; `total` receives the block's sum.
+__device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s_red, uint32_t &total) {
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    const uint32_t incl = warp_inclusive_sum(v);
+    if (lane == 31) s_red[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t t = s_red[w];
+        before += (uint32_t)w < warp ? t : 0u;
+        total += t;
+    }
+    __syncthreads();
+    return before + incl - v;
+}
+
+// Four counts starting at cell c (a multiple of 4), zeros past `hi`.
+__device__ __forceinline__ uint4 load_counts(const uint32_t *conteos, uint64_t c, uint64_t hi) {
+    if (c + 4 <= hi) return *reinterpret_cast<const uint4 *>(conteos + c);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (c < hi) v.x = conteos[c];
+    if (c + 1 < hi) v.y = conteos[c + 1];
+    if (c + 2 < hi) v.z = conteos[c + 2];
+    return v;
+}
+
+// inicios[c..c+3] = first, first + v.x, ... (only cells below `hi`).
+__device__ __forceinline__ void store_starts(uint32_t *inicios, uint64_t c, uint64_t hi, uint32_t first,
+                                             const uint4 &v) {
+    const uint4 o = make_uint4(first, first + v.x, first + v.x + v.y, first + v.x + v.y + v.z);
+    if (c + 4 <= hi) {
+        *reinterpret_cast<uint4 *>(inicios + c) = o;
+    } else {
+        if (c < hi) inicios[c] = o.x;
+        if (c + 1 < hi) inicios[c + 1] = o.y;
+        if (c + 2 < hi) inicios[c + 2] = o.z;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino,
+                   uint32_t *__restrict__ conteos, uint32_t *__restrict__ celdaDe,
+                   uint32_t *__restrict__ inicios, uint32_t *__restrict__ ordenado, uint32_t n,
+                   uint64_t cells, Geometry g, grid_ws_header *hdr, uint32_t *__restrict__ chunk_sums,
+                   uint32_t *__restrict__ slots) {
+    __shared__ uint32_t s_red[kWarps];
+    __shared__ uint4 s_held[kScanVecs][kThreads];  // this CTA's chunk of counts (32 KB)
+    const uint32_t tid = threadIdx.x;
+    const uint32_t lane = tid & 31u;
+    const uint64_t grid_threads = (uint64_t)gridDim.x * kThreads;
+    uint32_t gen = 0;
+    if (tid == 0) gen = load_acquire(&hdr->bar_gen);  // before this CTA's first arrival
+
+    UGRID_PHASE_MARK(0);
+    // ---- clear ---------------------------------------------------------------
+    {
+        const uint64_t quads = cells / 4;
+        uint4 *c4 = reinterpret_cast<uint4 *>(conteos);
+        for (uint64_t q = (uint64_t)blockIdx.x * kThreads + tid; q < quads; q += grid_threads)
+            c4[q] = make_uint4(0u, 0u, 0u, 0u);
+        for (uint64_t c = quads * 4 + (uint64_t)blockIdx.x * kThreads + tid; c < cells; c += grid_threads)
+            conteos[c] = 0u;
+    }
+    UGRID_PHASE_END(0);
+    grid_barrier(hdr, gen);
+
+    UGRID_PHASE_MARK(1);
+    // ---- count: cell, histogram and slot -------------------------------------
+    unsigned long long keep;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+        for (uint64_t r0 = (uint64_t)blockIdx.x * kThreads * kCountItems; r0 < n; r0 += grid_threads * kCountItems) {
+        uint4 rec[kCountItems];
+#pragma unroll
+        for (int k = 0; k < kCountItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+            if (i < n) rec[k] = load_policy(origen + 2 * i, keep);
+        }
+        uint32_t cell[kCountItems], peers[kCountItems], base[kCountItems];
+#pragma unroll
+        for (int k = 0; k < kCountItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+            const bool valid = i < n;
+            cell[k] = valid ? cell_of(rec[k], g) : 0u;
+            if (valid) celdaDe[i] = cell[k];
+            peers[k] = 1u << lane;
+            if (warp_has_adjacent_duplicates(valid, cell[k])) {
+                const uint32_t active = __ballot_sync(0xffffffffu, valid);
+                if (valid) peers[k] = __match_any_sync(active, cell[k]);
+            }
+            base[k] = 0;
+            if (valid && lane == (uint32_t)(__ffs(peers[k]) - 1))
+                base[k] = atomicAdd(conteos + cell[k], __popc(peers[k]));
+        }
+#pragma unroll
+        for (int k = 0; k < kCountItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+            const uint32_t slot = __shfl_sync(0xffffffffu, base[k], __ffs(peers[k]) - 1) +
+                                  __popc(peers[k] & lanemask_lt());
+            if (i < n) slots[i] = slot;
+        }
+    }
+    UGRID_PHASE_END(1);
+    grid_barrier(hdr, gen);
+
+    UGRID_PHASE_MARK(2);
+    // ---- scan a: chunk totals --------------------------------------------------
+    // Chunks are multiples of 4 cells so that 16-byte accesses stay aligned.
+    // When a chunk fits in kScanVecs vectors per thread its counts stay in
+    // shared memory for scan b; otherwise scan b reads them again.
+    const uint64_t chunk = ((cells + gridDim.x - 1) / gridDim.x + 3) & ~3ull;
+    const uint64_t lo = min((uint64_t)blockIdx.x * chunk, cells);
+    const uint64_t hi = min(lo + chunk, cells);
+    const bool resident = chunk <= 4ull * kThreads * kScanVecs;
+    {
+        uint32_t sum = 0;
+        if (resident) {
+            uint4 v[kScanVecs];
+#pragma unroll
+            for (int q = 0; q < kScanVecs; ++q) v[q] = load_counts(conteos, lo + 4ull * (q * kThreads + tid), hi);
+#pragma unroll
+            for (int q = 0; q < kScanVecs; ++q) {
+                s_held[q][tid] = v[q];
+                sum += v[q].x + v[q].y + v[q].z + v[q].w;
+            }
+        } else {
+            for (uint64_t c0 = lo; c0 < hi; c0 += 4ull * kThreads * kScanVecs) {
+                uint4 v[kScanVecs];
+#pragma unroll
+                for (int q = 0; q < kScanVecs; ++q) v[q] = load_counts(conteos, c0 + 4ull * (q * kThreads + tid), hi);
+#pragma unroll
+                for (int q = 0; q < kScanVecs; ++q) sum += v[q].x + v[q].y + v[q].z + v[q].w;
+            }
+        }
+        sum = block_sum(sum, s_red);
+        if (tid == 0) chunk_sums[blockIdx.x] = sum;
+    }
+    UGRID_PHASE_END(2);
+    grid_barrier(hdr, gen);
+
+    UGRID_PHASE_MARK(3);
+    // ---- scan b: exclusive scan of this chunk, offset by the earlier chunks ---
+    {
+        uint32_t before = 0;
+        for (uint32_t b = tid; b < blockIdx.x; b += kThreads) before += chunk_sums[b];
+        uint32_t prefix = block_sum(before, s_red);
+        for (uint64_t c0 = lo; c0 < hi; c0 += 4ull * kThreads * kScanVecs) {
+            uint4 v[kScanVecs];
+#pragma unroll
+            for (int q = 0; q < kScanVecs; ++q)
+                v[q] = resident ? s_held[q][tid] : load_counts(conteos, c0 + 4ull * (q * kThreads + tid), hi);
+#pragma unroll
+            for (int q = 0; q < kScanVecs; ++q) {
+                uint32_t total;
+                const uint32_t excl = block_exclusive_scan(v[q].x + v[q].y + v[q].z + v[q].w, s_red, total);
+                store_starts(inicios, c0 + 4ull * (q * kThreads + tid), hi, prefix + excl, v[q]);
+                prefix += total;
+            }
+        }
+        if (blockIdx.x == gridDim.x - 1 && tid == 0) inicios[cells] = prefix;
+    }
+    UGRID_PHASE_END(3);
+    grid_barrier(hdr, gen);
+
+    UGRID_PHASE_MARK(4);
+    // ---- scatter: every particle to its slot ----------------------------------
+    for (uint64_t r0 = (uint64_t)blockIdx.x * kThreads * kScatterItems; r0 < n;
+         r0 += grid_threads * kScatterItems) {
+        uint32_t cell[kScatterItems], slot[kScatterItems], start[kScatterItems];
+#pragma unroll
+        for (int k = 0; k < kScatterItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+            if (i < n) {
+                cell[k] = celdaDe[i];
+                slot[k] = slots[i];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kScatterItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+            if (i < n) start[k] = inicios[cell[k]];
+        }
+#pragma unroll
+        for (int k = 0; k < kScatterItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+            if (i < n) {
+                const uint32_t pos = start[k] + slot[k];
+                if (pos < n)
+                    ordenado[pos] = (uint32_t)i;
+                else
+                    record_status(&hdr->status, kStatusBounds);
+            }
+        }
+    }
+    UGRID_PHASE_END(4);
+    grid_barrier(hdr, gen);
+
+    UGRID_PHASE_MARK(5);
+    // ---- gather: two threads per 32-byte record -------------------------------
+    unsigned long long last_use;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(last_use));
+    const uint64_t halves = 2ull * n;
+    for (uint64_t r0 = (uint64_t)blockIdx.x * kThreads * kGatherItems; r0 < halves; r0 += grid_threads * kGatherItems) {
+        uint32_t src[kGatherItems];
+#pragma unroll
+        for (int k = 0; k < kGatherItems; ++k) {
+            const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+            src[k] = h < halves ? ordenado[h >> 1] : 0u;
+        }
+        uint4 v[kGatherItems];
+#pragma unroll
+        for (int k = 0; k < kGatherItems; ++k) {
+            const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+            if (h < halves && src[k] < n) v[k] = load_policy(origen + 2 * (uint64_t)src[k] + (h & 1), last_use);
+        }
+#pragma unroll
+        for (int k = 0; k < kGatherItems; ++k) {
+            const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+            if (h < halves) {
+                if (src[k] < n)
+                    store_cs(destino + h, v[k]);
+                else if ((h & 1) == 0)
+                    record_status(&hdr->status, kStatusBounds);
+            }
+        }
+    }
+    UGRID_PHASE_MARK(6);
+}
+
+std::atomic<int> g_grid[kMaxDevices];  // cached grid size per device (0 = not yet known)
+
+cudaError_t fused_grid(int device, int *grid) {
+    if (device >= 0 && device < kMaxDevices) {
+        const int cached = g_grid[device].load(std::memory_order_relaxed);
+        if (cached != 0) {
+            *grid = cached;
+            return cached > 0 ? cudaSuccess : cudaErrorNotSupported;
+        }
+    }
+    int coop = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_fused_kernel, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    int g = coop ? per_sm * sms : -1;
+    if (g == 0) g = -1;
+    if (g > (int)kFusedMaxCtas) g = (int)kFusedMaxCtas;
+    if (device >= 0 && device < kMaxDevices) g_grid[device].store(g, std::memory_order_relaxed);
+    *grid = g;
+    return g > 0 ? cudaSuccess : cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *destino,
+                               uint32_t *conteos, uint32_t *celdaDe, uint32_t *inicios,
+                               uint32_t *ordenado, uint32_t n, uint64_t cells, const Geometry &g,
+                               grid_ws_header *hdr, uint32_t *chunk_sums, uint32_t *slots,
+                               cudaStream_t s) {
+    int device = 0, grid = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e == cudaSuccess) e = fused_grid(device, &grid);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, build_fused_kernel, reinterpret_cast<const uint4 *>(origen),
+                              reinterpret_cast<uint4 *>(destino), conteos, celdaDe, inicios, ordenado,
+                              n, cells, g, hdr, chunk_sums, slots);
+}
+
+}  // namespace ugrid

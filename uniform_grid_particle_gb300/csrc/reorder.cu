@@ -19,6 +19,8 @@ constexpr int kItems = 4;  // half-records per thread, loads issued before store
 __global__ void __launch_bounds__(kThreads)
 reorder_kernel(const uint32_t *__restrict__ ordenado, const uint4 *__restrict__ origen,
                uint4 *__restrict__ destino, uint32_t n, uint32_t *status) {
+    allow_dependent_launch();
+    grid_dependency_wait();
     const uint64_t first = (uint64_t)blockIdx.x * (kThreads * kItems) + threadIdx.x;
     uint32_t src[kItems];
 #pragma unroll
@@ -47,14 +49,15 @@ reorder_kernel(const uint32_t *__restrict__ ordenado, const uint4 *__restrict__ 
 }  // namespace
 
 cudaError_t launch_reorder(const uint32_t *ordenado, const ugrid_particula *origen,
-                           ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s) {
+                           ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s,
+                           bool pdl) {
     if (n == 0) return cudaSuccess;
     const uint64_t halves = 2ull * n;
     const uint64_t per_block = (uint64_t)kThreads * kItems;
     const unsigned blocks = (unsigned)((halves + per_block - 1) / per_block);
-    reorder_kernel<<<blocks, kThreads, 0, s>>>(ordenado, reinterpret_cast<const uint4 *>(origen),
-                                               reinterpret_cast<uint4 *>(destino), n, status);
-    return cudaGetLastError();
+    return launch(reorder_kernel, blocks, kThreads, 0, s, pdl, ordenado,
+                  reinterpret_cast<const uint4 *>(origen), reinterpret_cast<uint4 *>(destino), n,
+                  status);
 }
 
 }  // namespace ugrid

@@ -5,17 +5,24 @@
 // inicios[C] = N so that the end of cell c is inicios[c + 1].
 //
 // The pages use a three-level tree of 512-wide blocks (six dispatches).  Here
-// it is one pass: tiles of 4096 cells, each CTA takes a tile ticket in arrival
+// it is one pass: tiles of 8192 cells, each CTA takes a tile ticket in arrival
 // order, publishes its tile total, and finds its exclusive prefix by looking
 // back over its predecessors' published words (decoupled look-back, Merrill &
 // Garland, "Single-pass Parallel Prefix Scan with Decoupled Look-back", 2016).
 //
 // Look-back words are 64-bit: flag in the high half (0 = not yet published,
 // 1 = tile total only, 2 = inclusive prefix), value in the low half, written
-// and read with single relaxed gpu-scope accesses.  Every wait gives up after
-// kSpinLimitNs, records kStatusTimeout and carries on with a zero prefix, so
-// a kernel never hangs.  The last CTA to finish zeroes the words and the
-// counters, leaving the workspace ready for the next call.
+// and read with single relaxed gpu-scope accesses.  One warp looks back over
+// 256 predecessors per round (8 words per lane), so while all tiles of a
+// 2M-cell grid are in flight a single round reaches tile 0; only that warp
+// polls, which keeps the few L2 lines holding the words from becoming a hot
+// spot.  Every wait gives up after kSpinLimitNs, records kStatusTimeout and
+// carries on with a zero prefix, so a kernel never hangs.  The last CTA to
+// finish zeroes the words and the counters, leaving the workspace ready for
+// the next call.
+//
+// Each tile is four rows of 2048 cells; thread t holds cells 4t..4t+3 of every
+// row, so each row is read and written with fully coalesced 16-byte accesses.
 //
 // With zero_input (used by grid_build) each CTA also writes zeros over its
 // tile of conteos after reading it: that is the second clear of the pages
@@ -29,6 +36,9 @@ constexpr unsigned long long kFlagAggregate = 1ull << 32;
 constexpr unsigned long long kFlagPrefix = 2ull << 32;
 constexpr uint32_t kFullMask = 0xffffffffu;
 constexpr int kWarps = kScanThreads / 32;
+constexpr int kRows = kScanItems / 4;
+constexpr uint32_t kRowCells = kScanThreads * 4;
+constexpr int kLookWords = 8;  // predecessors per lane per look-back round
 
 __device__ __forceinline__ unsigned long long load_relaxed(const unsigned long long *p) {
     unsigned long long v;
@@ -50,134 +60,156 @@ __device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v) {
     return v;
 }
 
-// Exclusive prefix of `tile` from its predecessors' words; called by one
-// full warp.  Lane l inspects tile j - l, 32 tiles per round, until some
-// predecessor shows an inclusive prefix.
+// Exclusive prefix of `tile` from its predecessors' words; called by one full
+// warp.  Word w of lane l is predecessor j - (w*32 + l): the nearest one that
+// shows an inclusive prefix ends the walk, and the tile totals of the closer
+// ones are added to it.
 __device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t tile,
                               uint32_t *status_word) {
     const uint32_t lane = lane_id();
     uint32_t exclusive = 0;
     long long j = (long long)tile - 1;
-    unsigned long long start = 0;
     while (true) {
-        const long long idx = j - (long long)lane;
-        unsigned long long s = idx >= 0 ? load_relaxed(tile_status + idx) : kFlagPrefix;
-        while (__any_sync(kFullMask, (s >> 32) == 0)) {
-            if (start == 0) start = global_ns();
-            const bool give_up = __shfl_sync(kFullMask, (global_ns() - start) > kSpinLimitNs, 0);
-            if (give_up) {
-                if ((s >> 32) == 0) s = kFlagPrefix;  // carry on with a zero prefix
-                if (lane == 0) record_status(status_word, kStatusTimeout);
-                break;
+        unsigned long long s[kLookWords];
+#pragma unroll
+        for (int w = 0; w < kLookWords; ++w) {
+            const long long idx = j - (long long)(w * 32 + lane);
+            s[w] = idx >= 0 ? load_relaxed(tile_status + idx) : kFlagPrefix;
+        }
+#pragma unroll
+        for (int w = 0; w < kLookWords; ++w) {
+            if ((s[w] >> 32) == 0) {
+                const long long idx = j - (long long)(w * 32 + lane);
+                const unsigned long long start = global_ns();
+                do {
+                    __nanosleep(64);
+                    s[w] = load_relaxed(tile_status + idx);
+                    if ((s[w] >> 32) == 0 && global_ns() - start > kSpinLimitNs) {
+                        record_status(status_word, kStatusTimeout);
+                        s[w] = kFlagPrefix;  // give up: carry on with a zero prefix
+                    }
+                } while ((s[w] >> 32) == 0);
             }
-            __nanosleep(32);
-            if ((s >> 32) == 0) s = load_relaxed(tile_status + idx);
         }
-        const uint32_t prefix_lanes = __ballot_sync(kFullMask, (s >> 32) == 2);
-        uint32_t value = (uint32_t)s;
-        if (prefix_lanes) {
-            const uint32_t stop = (uint32_t)(__ffs(prefix_lanes) - 1);
-            if (lane > stop) value = 0;
-            return exclusive + __reduce_add_sync(kFullMask, value);
-        }
-        exclusive += __reduce_add_sync(kFullMask, value);
-        j -= 32;
+        // Position (w*32 + lane) of the nearest inclusive prefix in the window.
+        uint32_t nearest = 0xffffffffu;
+#pragma unroll
+        for (int w = kLookWords - 1; w >= 0; --w)
+            if ((s[w] >> 32) == 2) nearest = (uint32_t)(w * 32) + lane;
+        nearest = __reduce_min_sync(kFullMask, nearest);
+        uint32_t sum = 0;
+#pragma unroll
+        for (int w = 0; w < kLookWords; ++w)
+            if ((uint32_t)(w * 32) + lane <= nearest) sum += (uint32_t)s[w];
+        exclusive += __reduce_add_sync(kFullMask, sum);
+        if (nearest != 0xffffffffu) return exclusive;
+        j -= 32 * kLookWords;
     }
 }
 
+// kZeroInput is the grid_build variant: it zeroes conteos after reading it,
+// and it takes its tile ticket before waiting for the previous kernel (the
+// count, which does not touch the workspace; the build's leading memset has
+// already ordered it after any earlier scan on this workspace).
 template <bool kZeroInput>
 __global__ void __launch_bounds__(kScanThreads)
 scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, uint32_t tiles,
             grid_ws_header *hdr, unsigned long long *tile_status) {
     __shared__ uint32_t s_tile;
-    __shared__ uint32_t s_warp[kWarps];
-    __shared__ uint32_t s_total;
+    __shared__ uint32_t s_warp[kRows][kWarps];
+    __shared__ uint32_t s_row[kRows];
     __shared__ uint32_t s_prefix;
     __shared__ uint32_t s_last;
     const uint32_t tid = threadIdx.x;
     const uint32_t lane = tid & 31u;
     const uint32_t warp = tid >> 5;
 
+    allow_dependent_launch();
+    if (!kZeroInput) grid_dependency_wait();
     if (tid == 0) s_tile = atomicAdd(&hdr->scan_ticket, 1u);
+    if (kZeroInput) grid_dependency_wait();
     __syncthreads();
     const uint32_t tile = s_tile;
 
     if (tile < tiles) {
-        const uint64_t base = (uint64_t)tile * kScanTile + (uint64_t)tid * kScanItems;
-        const bool full = base + kScanItems <= cells;
-        uint32_t v[kScanItems];
-        if (full) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(conteos + base);
+        const uint64_t tile_base = (uint64_t)tile * kScanTile;
+        uint4 v[kRows];
 #pragma unroll
-            for (int q = 0; q < kScanItems / 4; ++q) {
-                const uint4 x = src[q];
-                v[4 * q + 0] = x.x;
-                v[4 * q + 1] = x.y;
-                v[4 * q + 2] = x.z;
-                v[4 * q + 3] = x.w;
+        for (int r = 0; r < kRows; ++r) {
+            const uint64_t c = tile_base + (uint64_t)r * kRowCells + 4u * tid;
+            if (c + 4 <= cells) {
+                v[r] = *reinterpret_cast<const uint4 *>(conteos + c);
+            } else {
+                v[r].x = c + 0 < cells ? conteos[c + 0] : 0u;
+                v[r].y = c + 1 < cells ? conteos[c + 1] : 0u;
+                v[r].z = c + 2 < cells ? conteos[c + 2] : 0u;
+                v[r].w = c + 3 < cells ? conteos[c + 3] : 0u;
             }
-        } else {
-#pragma unroll
-            for (int k = 0; k < kScanItems; ++k) v[k] = base + k < cells ? conteos[base + k] : 0u;
         }
-        // Thread-local exclusive scan; `run` is the thread's total.
-        uint32_t run = 0;
+        // Per row: the thread's total, its exclusive prefix inside the row.
+        uint32_t total[kRows], excl[kRows];
 #pragma unroll
-        for (int k = 0; k < kScanItems; ++k) {
-            const uint32_t t = v[k];
-            v[k] = run;
-            run += t;
+        for (int r = 0; r < kRows; ++r) {
+            total[r] = v[r].x + v[r].y + v[r].z + v[r].w;
+            const uint32_t incl = warp_inclusive_sum(total[r]);
+            excl[r] = incl - total[r];
+            if (lane == 31) s_warp[r][warp] = incl;
         }
-        // Block-wide exclusive scan of the thread totals.
-        const uint32_t incl = warp_inclusive_sum(run);
-        if (lane == 31) s_warp[warp] = incl;
         __syncthreads();
-        if (warp == 0) {
-            const uint32_t w = lane < kWarps ? s_warp[lane] : 0u;
+        if (warp < kRows) {  // warp r scans the warp totals of row r
+            const uint32_t w = lane < kWarps ? s_warp[warp][lane] : 0u;
             const uint32_t wi = warp_inclusive_sum(w);
-            if (lane < kWarps) s_warp[lane] = wi - w;
-            if (lane == kWarps - 1) s_total = wi;
+            if (lane < kWarps) s_warp[warp][lane] = wi - w;
+            if (lane == kWarps - 1) s_row[warp] = wi;
         }
         __syncthreads();
-        const uint32_t thread_excl = s_warp[warp] + incl - run;
+        uint32_t row_off[kRows];
+        uint32_t tile_total = 0;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            row_off[r] = tile_total;
+            tile_total += s_row[r];
+        }
 
         // Publish the tile total, then find the prefix of all earlier tiles.
         if (warp == 0) {
-            const uint32_t total = s_total;
             uint32_t exclusive = 0;
             if (tile == 0) {
-                if (lane == 0) store_relaxed(tile_status, kFlagPrefix | total);
+                if (lane == 0) store_relaxed(tile_status, kFlagPrefix | tile_total);
             } else {
-                if (lane == 0) store_relaxed(tile_status + tile, kFlagAggregate | total);
+                if (lane == 0) store_relaxed(tile_status + tile, kFlagAggregate | tile_total);
                 exclusive = look_back(tile_status, tile, &hdr->status);
-                if (lane == 0) store_relaxed(tile_status + tile, kFlagPrefix | (uint32_t)(exclusive + total));
+                if (lane == 0)
+                    store_relaxed(tile_status + tile, kFlagPrefix | (uint32_t)(exclusive + tile_total));
             }
             if (lane == 0) s_prefix = exclusive;
         }
         __syncthreads();
 
-        const uint32_t prefix = s_prefix + thread_excl;
-        if (full) {
-            uint4 *dst = reinterpret_cast<uint4 *>(inicios + base);
+        const uint32_t prefix = s_prefix;
 #pragma unroll
-            for (int q = 0; q < kScanItems / 4; ++q)
-                dst[q] = make_uint4(prefix + v[4 * q], prefix + v[4 * q + 1], prefix + v[4 * q + 2],
-                                    prefix + v[4 * q + 3]);
-            if (kZeroInput) {
-                uint4 *z = reinterpret_cast<uint4 *>(conteos + base);
+        for (int r = 0; r < kRows; ++r) {
+            const uint64_t c = tile_base + (uint64_t)r * kRowCells + 4u * tid;
+            uint4 o;
+            o.x = prefix + row_off[r] + s_warp[r][warp] + excl[r];
+            o.y = o.x + v[r].x;
+            o.z = o.y + v[r].y;
+            o.w = o.z + v[r].z;
+            if (c + 4 <= cells) {
+                *reinterpret_cast<uint4 *>(inicios + c) = o;
+                if (kZeroInput) *reinterpret_cast<uint4 *>(conteos + c) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                const uint32_t ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-                for (int q = 0; q < kScanItems / 4; ++q) z[q] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < kScanItems; ++k) {
-                if (base + k < cells) {
-                    inicios[base + k] = prefix + v[k];
-                    if (kZeroInput) conteos[base + k] = 0u;
+                for (int k = 0; k < 4; ++k) {
+                    if (c + k < cells) {
+                        inicios[c + k] = ov[k];
+                        if (kZeroInput) conteos[c + k] = 0u;
+                    }
                 }
             }
         }
-        if (tile == tiles - 1 && tid == 0) inicios[cells] = s_prefix + s_total;
+        if (tile == tiles - 1 && tid == 0) inicios[cells] = prefix + tile_total;
     } else if (tid == 0) {
         record_status(&hdr->status, kStatusBounds);  // more CTAs than tiles: a stale ticket
     }
@@ -202,13 +234,14 @@ scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, u
 }  // namespace
 
 cudaError_t launch_scan(uint32_t *conteos, uint32_t *inicios, uint64_t cells, bool zero_input,
-                        grid_ws_header *hdr, unsigned long long *tile_status, cudaStream_t s) {
+                        grid_ws_header *hdr, unsigned long long *tile_status, cudaStream_t s,
+                        bool pdl) {
     const uint32_t tiles = (uint32_t)scan_tiles(cells);
     if (zero_input)
-        scan_kernel<true><<<tiles, kScanThreads, 0, s>>>(conteos, inicios, cells, tiles, hdr, tile_status);
-    else
-        scan_kernel<false><<<tiles, kScanThreads, 0, s>>>(conteos, inicios, cells, tiles, hdr, tile_status);
-    return cudaGetLastError();
+        return launch(scan_kernel<true>, tiles, kScanThreads, 0, s, pdl, conteos, inicios, cells,
+                      tiles, hdr, tile_status);
+    return launch(scan_kernel<false>, tiles, kScanThreads, 0, s, pdl, conteos, inicios, cells,
+                  tiles, hdr, tile_status);
 }
 
 }  // namespace ugrid

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(kSmallThreads)
 segment_small_kernel(const uint32_t *__restrict__ inicios, uint32_t *__restrict__ ordenado,
                      uint32_t n, uint32_t cells, grid_ws_header *hdr, uint32_t *queue,
                      uint32_t queue_capacity) {
+    allow_dependent_launch();
+    grid_dependency_wait();
     const uint64_t c = (uint64_t)blockIdx.x * kSmallThreads + threadIdx.x;
     if (c >= cells) return;
     const uint32_t a = inicios[c];
@@ -187,6 +189,8 @@ segment_big_kernel(const uint32_t *__restrict__ inicios, uint32_t *__restrict__ 
                    uint32_t queue_capacity, uint32_t *scratch) {
     extern __shared__ uint32_t smem[];
     __shared__ uint32_t s_last;
+    allow_dependent_launch();
+    grid_dependency_wait();
     const uint32_t queued = *(volatile uint32_t *)&hdr->stable_big;
     const uint32_t count = queued < queue_capacity ? queued : queue_capacity;
     for (uint32_t q = blockIdx.x; q < count; q += gridDim.x) {
@@ -223,13 +227,12 @@ size_t segment_queue_capacity(uint64_t n, uint64_t cells) {
 
 cudaError_t launch_segment_sort(const uint32_t *inicios, uint32_t *ordenado, uint32_t n,
                                 uint32_t cells, grid_ws_header *hdr, uint32_t *queue,
-                                uint32_t *scratch, cudaStream_t s) {
+                                uint32_t *scratch, cudaStream_t s, bool pdl) {
     if (n < 2) return cudaSuccess;
     const uint32_t capacity = (uint32_t)segment_queue_capacity(n, cells);
     const unsigned small_blocks = (unsigned)((cells + kSmallThreads - 1) / kSmallThreads);
-    segment_small_kernel<<<small_blocks, kSmallThreads, 0, s>>>(inicios, ordenado, n, cells, hdr,
-                                                                 queue, capacity);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch(segment_small_kernel, small_blocks, kSmallThreads, 0, s, pdl, inicios,
+                           ordenado, n, cells, hdr, queue, capacity);
     if (e != cudaSuccess) return e;
     int device = 0, sms = 0;
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
@@ -238,9 +241,8 @@ cudaError_t launch_segment_sort(const uint32_t *inicios, uint32_t *ordenado, uin
     if ((e = cudaFuncSetAttribute(segment_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kBigSmemBytes)) != cudaSuccess)
         return e;
-    segment_big_kernel<<<(unsigned)sms, kBigThreads, kBigSmemBytes, s>>>(inicios, ordenado, n, hdr,
-                                                                         queue, capacity, scratch);
-    return cudaGetLastError();
+    return launch(segment_big_kernel, (unsigned)sms, kBigThreads, kBigSmemBytes, s, pdl, inicios,
+                  ordenado, n, hdr, queue, capacity, scratch);
 }
 
 }  // namespace ugrid

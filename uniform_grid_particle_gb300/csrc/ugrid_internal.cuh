@@ -25,44 +25,79 @@ struct Geometry {
 };
 
 // ---- scan tiling --------------------------------------------------------
-constexpr int kScanThreads = 256;
+constexpr int kScanThreads = 512;
 constexpr int kScanItems = 16;  // four 16-byte vectors per thread
-constexpr uint32_t kScanTile = kScanThreads * kScanItems;  // 4096 cells
+constexpr uint32_t kScanTile = kScanThreads * kScanItems;  // 8192 cells
 
 inline uint64_t scan_tiles(uint64_t cells) { return (cells + kScanTile - 1) / kScanTile; }
 
 // ---- workspace layout ---------------------------------------------------
 constexpr size_t kHeaderBytes = 256;
+constexpr uint32_t kFusedMaxCtas = 4096;  // bound on the fused build's grid
 struct WsLayout {
     size_t tile_status;     // u64[tiles]
+    size_t chunk_sums;      // u32[kFusedMaxCtas] per-CTA cell-chunk totals (fused build)
+    size_t slots;           // u32[n] slot of each particle in its cell (fused build)
     size_t stable_queue;    // u32[cells] queue of long segments (GRID_STABLE)
     size_t stable_scratch;  // u32[n] radix-sort scratch (GRID_STABLE)
     size_t total;
 };
 WsLayout ws_layout(uint64_t n, uint64_t cells, unsigned flags);
 
+// ---- launch helper --------------------------------------------------------
+// With `pdl` the kernel may be launched while the previous kernel on the
+// stream is still running (programmatic dependent launch); every kernel
+// starts with grid_dependency_wait() before it touches memory the previous
+// kernel wrote, so results are the same either way.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                   cudaStream_t s, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- launchers (one per kernel family); all enqueue on `s` --------------
 cudaError_t launch_count(const ugrid_particula *parts, uint32_t *conteos, uint32_t *celdaDe,
-                         uint32_t n, const Geometry &g, cudaStream_t s);
+                         uint32_t n, const Geometry &g, cudaStream_t s, bool pdl);
 
 // inicios = exclusive scan of conteos (C+1 entries).  When zero_input is
 // true the kernel also writes zeros over each conteos tile after reading it.
 cudaError_t launch_scan(uint32_t *conteos, uint32_t *inicios, uint64_t cells, bool zero_input,
-                        grid_ws_header *hdr, unsigned long long *tile_status, cudaStream_t s);
+                        grid_ws_header *hdr, unsigned long long *tile_status, cudaStream_t s,
+                        bool pdl);
 
 cudaError_t launch_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cursor,
                            uint32_t *ordenado, uint32_t n, uint32_t cells, uint32_t *status,
-                           cudaStream_t s);
+                           cudaStream_t s, bool pdl);
 
 cudaError_t launch_reorder(const uint32_t *ordenado, const ugrid_particula *origen,
-                           ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s);
+                           ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s,
+                           bool pdl);
+
+// The whole non-stable build in one cooperative launch (see build_fused.cu).
+// Returns cudaErrorNotSupported when the device cannot run it, so the caller
+// can fall back to one launch per phase.
+cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *destino,
+                               uint32_t *conteos, uint32_t *celdaDe, uint32_t *inicios,
+                               uint32_t *ordenado, uint32_t n, uint64_t cells, const Geometry &g,
+                               grid_ws_header *hdr, uint32_t *chunk_sums, uint32_t *slots,
+                               cudaStream_t s);
 
 // Queue entries needed for cells longer than the register tier (<= cells).
 size_t segment_queue_capacity(uint64_t n, uint64_t cells);
 
 cudaError_t launch_segment_sort(const uint32_t *inicios, uint32_t *ordenado, uint32_t n,
                                 uint32_t cells, grid_ws_header *hdr, uint32_t *queue,
-                                uint32_t *scratch, cudaStream_t s);
+                                uint32_t *scratch, cudaStream_t s, bool pdl);
 
 // ---- device helpers -----------------------------------------------------
 __device__ __forceinline__ void record_status(uint32_t *status, uint32_t bit) {
@@ -70,6 +105,47 @@ __device__ __forceinline__ void record_status(uint32_t *status, uint32_t bit) {
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// Clamped cell coordinate along one axis ("Contar partículas por celda",
+// §El kernel: the range guard lives in the cell-index helper):
+// floor((p - o) * invCell) in fp32, round-to-nearest subtraction and
+// multiplication (never contracted), saturated to [0, dim - 1].  `f >= 0` is
+// false for NaN, so NaN goes to 0; the float-to-unsigned conversion saturates
+// +inf and huge values, and the min() brings them to dim - 1.
+__device__ __forceinline__ uint32_t axis_coord(float p, float o, float inv, uint32_t dim) {
+    const float f = floorf(__fmul_rn(__fsub_rn(p, o), inv));
+    return f >= 0.0f ? min(__float2uint_rz(f), dim - 1u) : 0u;
+}
+
+// Linear cell index x + y*GX + z*GX*GY ("Reordenar por celda…", §El orden de
+// las celdas) of the position in the first 16 bytes of a record.
+__device__ __forceinline__ uint32_t cell_of(const uint4 &rec, const Geometry &g) {
+    const uint32_t x = axis_coord(__uint_as_float(rec.x), g.origin[0], g.inv_cell, g.dims[0]);
+    const uint32_t y = axis_coord(__uint_as_float(rec.y), g.origin[1], g.inv_cell, g.dims[1]);
+    const uint32_t z = axis_coord(__uint_as_float(rec.z), g.origin[2], g.inv_cell, g.dims[2]);
+    return x + g.dims[0] * (y + g.dims[1] * z);
+}
+
+// True (for the whole warp) when some valid lane holds the same key as the
+// valid lane just below it: the cheap test that decides whether grouping the
+// warp's atomics by key with __match_any_sync is worth it.
+__device__ __forceinline__ bool warp_has_adjacent_duplicates(bool valid, uint32_t key) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t active = __ballot_sync(0xffffffffu, valid);
+    const uint32_t below = __shfl_up_sync(0xffffffffu, key, 1);
+    const bool dup = valid && lane > 0 && ((active >> (lane - 1)) & 1u) && below == key;
+    return __any_sync(0xffffffffu, dup);
+}
+
+// Programmatic dependent launch: wait for the previous grid's memory to be
+// visible (a no-op when the kernel was launched normally), and let the next
+// grid begin launching once every CTA of this one has started.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
