@@ -74,7 +74,8 @@ enum grid_status_code {
     GRID_EINVAL = 1,   /* bad arguments; nothing was enqueued */
     GRID_ECUDA = 2,    /* a CUDA call or kernel launch failed */
     GRID_ETIMEOUT = 3, /* (grid_status) a device-side wait gave up */
-    GRID_EBOUNDS = 4   /* (grid_status) an index read from an input was out of range */
+    GRID_EBOUNDS = 4,  /* (grid_status) an index read from an input was out of range */
+    GRID_ERANGE = 5    /* (grid_scan_noalloc) more cells than its fixed scratch serves */
 };
 
 /* flags */
@@ -168,6 +169,30 @@ int grid_reorder(const uint32_t *ordenado, const ugrid_particula *origen, ugrid_
 int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
                uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, void *ws,
                unsigned flags, const grid_params *p, void *stream);
+
+/* Exclusive scan for callers that cannot allocate device memory; the pages
+ * have no counterpart to it.  It computes exactly what grid_scan computes
+ * (inicios[0] = 0, inicios[c+1] = inicios[c] + conteos[c], inicios[C] = N),
+ * but keeps the scan's scratch — a 256-byte header and one 64-bit look-back
+ * word per 8192-cell tile — in a fixed 33,024-byte array inside the library
+ * instead of a caller workspace.  It is meant for code that may not take
+ * device memory itself: an engine that owns every device buffer and hands
+ * them out from its own pool, or a per-frame step that cannot risk cudaMalloc
+ * stalling the device.  It allocates nothing and calls no allocating routine.
+ *   conteos  u32[C], read only; inicios u32[C+1], written; both device
+ *            pointers, 16-byte aligned, not overlapping.
+ *   p        as for grid_scan; celdas must be at most 33,554,432 (4096 tiles),
+ *            otherwise GRID_ERANGE is returned and nothing is enqueued.
+ * Returns GRID_OK, GRID_EINVAL (bad params or arrays, nothing enqueued),
+ * GRID_ERANGE, or GRID_ECUDA.  The first call on each device (with that
+ * device current) looks up the array's device address and caches it; make
+ * that first call before capturing any stream.  All calls share the one
+ * array, which each call clears on its stream before use: calls whose work
+ * overlaps on the GPU race on it and must be ordered by the caller.  A
+ * device-side wait that gives up is recorded only in that array and is not
+ * reported. */
+int grid_scan_noalloc(const uint32_t *conteos, uint32_t *inicios, const grid_params *p,
+                      void *stream);
 
 /* Synchronise `stream`, read and clear the workspace status word, and return
  * GRID_OK, GRID_ETIMEOUT (bit 0 set) or GRID_EBOUNDS (bit 1 set); GRID_ECUDA

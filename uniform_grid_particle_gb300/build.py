@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libugrid.so")
 
-SOURCES = ["abi.cu", "build_fused.cu", "count.cu", "scan.cu", "scatter.cu", "reorder.cu", "segsort.cu"]
+SOURCES = ["abi.cu", "build_fused.cu", "count.cu", "scan.cu", "scatter.cu", "reorder.cu", "segsort.cu",
+           "scan_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "ugrid_internal.cuh"), os.path.join(INCLUDE, "ugrid.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -254,6 +254,7 @@ const char *grid_error_string(int code) {
         case GRID_ECUDA: return "a CUDA call or kernel launch failed";
         case GRID_ETIMEOUT: return "a device-side wait timed out";
         case GRID_EBOUNDS: return "an index read from an input was out of range";
+        case GRID_ERANGE: return "more cells than the fixed scratch of grid_scan_noalloc serves";
         default: return "unknown status code";
     }
 }

@@ -21,7 +21,7 @@ import torch
 
 from . import build as _build
 
-GRID_OK, GRID_EINVAL, GRID_ECUDA, GRID_ETIMEOUT, GRID_EBOUNDS = 0, 1, 2, 3, 4
+GRID_OK, GRID_EINVAL, GRID_ECUDA, GRID_ETIMEOUT, GRID_EBOUNDS, GRID_ERANGE = 0, 1, 2, 3, 4, 5
 GRID_STABLE = 1
 
 _U32_DTYPES = (torch.int32, getattr(torch, "uint32", torch.int32))
@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "grid_reorder": ([vp, vp, vp, vp, pp, vp], ctypes.c_int),
             "grid_build": ([vp, vp, vp, vp, vp, vp, vp, u, pp, vp], ctypes.c_int),
             "grid_status": ([vp, vp], ctypes.c_int),
+            "grid_scan_noalloc": ([vp, vp, pp, vp], ctypes.c_int),
             "grid_error_string": ([ctypes.c_int], ctypes.c_char_p),
         }
         for name, (args, res) in sigs.items():
@@ -182,6 +183,15 @@ def grid_build(origen, destino, conteos, celdaDe, inicios, ordenado, ws, p: grid
                             _u32(conteos, "conteos", p.celdas), _u32(celdaDe, "celdaDe", p.conteo),
                             _u32(inicios, "inicios", p.celdas + 1), _u32(ordenado, "ordenado", p.conteo),
                             _ws(ws), flags, ctypes.byref(p), _stream(stream)), "grid_build")
+
+
+def grid_scan_noalloc(conteos, inicios, p: grid_params, stream=None) -> None:
+    """The scan of grid_scan for callers that cannot allocate: its scratch is a
+    fixed array inside the library (at most 33,554,432 cells; calls that
+    overlap on the GPU race on it)."""
+    _check(lib().grid_scan_noalloc(_u32(conteos, "conteos", p.celdas),
+                                   _u32(inicios, "inicios", p.celdas + 1), ctypes.byref(p),
+                                   _stream(stream)), "grid_scan_noalloc")
 
 
 def grid_status(ws, stream=None) -> int:
