@@ -95,15 +95,16 @@ typedef struct grid_ws_header {
     uint32_t scan_done;    /* tiles finished by the running scan; 0 between calls */
     uint32_t stable_big;   /* cells queued for the long-segment sort; 0 between calls */
     uint32_t stable_done;  /* CTAs finished by the running long-segment sort; 0 between calls */
-    uint32_t bar_count;    /* CTAs arrived at the fused build's current grid barrier; 0 between calls */
-    uint32_t bar_gen;      /* grid barrier generation (only ever incremented) */
-    uint32_t reserved[57];
+    uint32_t bar_count;    /* grid-barrier arrivals of the running fused build; 0 between calls */
+    uint32_t bar_exit;     /* CTAs that finished the running fused build; 0 between calls */
+    uint32_t counts_clean; /* cells of the fused build's counter array known to be zero */
+    uint32_t reserved[56];
 } grid_ws_header;
 
 /* Bytes of device workspace the calls below need for these params and flags
  * (the header, the scan's per-tile look-back status words, grid_build's
- * per-CTA chunk sums and per-particle slots and, with GRID_STABLE, the
- * segment-sort queue and scratch).  Returns 0 for invalid
+ * per-CTA chunk sums, per-particle slots and per-cell counter array and, with
+ * GRID_STABLE, the segment-sort queue and scratch).  Returns 0 for invalid
  * params.  The workspace must be 256-byte aligned and zero-filled once after
  * allocation (grid_workspace_init does that); every call leaves it ready for
  * the next one.  A workspace sized for one params/flags is valid for any

@@ -43,8 +43,10 @@ def test_workspace_bytes(L):
     p = P(L, 1_000_000, (128, 128, 128), cs=0.078125)
     tiles = (128 ** 3 + 8191) // 8192       # scan tiles of 8192 cells
     r256 = lambda b: (b + 255) // 256 * 256                     # noqa: E731
-    # header, look-back words, per-CTA chunk sums (up to 4096 CTAs), per-particle slots
-    assert L.grid_workspace_bytes(p, 0) == 256 + r256(tiles * 8) + r256(4096 * 4) + r256(4 * 1_000_000)
+    # header, look-back words, per-CTA chunk sums (up to 4096 CTAs), per-particle slots,
+    # per-cell counters of the fused build
+    assert L.grid_workspace_bytes(p, 0) == (256 + r256(tiles * 8) + r256(4096 * 4) + r256(4 * 1_000_000)
+                                            + r256(4 * 128 ** 3))
     stable = L.grid_workspace_bytes(p, L.GRID_STABLE)
     assert stable >= L.grid_workspace_bytes(p, 0) + 4 * 1_000_000
     assert L.grid_workspace_bytes(p, 2) == 0            # unknown flag
@@ -52,7 +54,7 @@ def test_workspace_bytes(L):
     bad.celdas = 7
     assert L.grid_workspace_bytes(bad, 0) == 0
     tiny = P(L, 0, (1, 1, 1), cs=1.0)
-    assert L.grid_workspace_bytes(tiny, 0) == 512 + 4096 * 4
+    assert L.grid_workspace_bytes(tiny, 0) == 512 + 4096 * 4 + 256
 
 
 def test_error_strings(L):

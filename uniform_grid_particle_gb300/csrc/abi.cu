@@ -19,6 +19,8 @@ WsLayout ws_layout(uint64_t n, uint64_t cells, unsigned flags) {
     off = round_up(off + kFusedMaxCtas * sizeof(uint32_t), 256);
     l.slots = off;
     off = round_up(off + n * sizeof(uint32_t), 256);
+    l.counts = off;
+    off = round_up(off + cells * sizeof(uint32_t), 256);
     if (flags & GRID_STABLE) {
         l.stable_queue = off;
         off = round_up(off + segment_queue_capacity(n, cells) * sizeof(uint32_t), 256);
@@ -208,7 +210,8 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
         const cudaError_t f = launch_build_fused(
             origen, destino, conteos, celdaDe, inicios, ordenado, p->conteo, c, g, h,
             reinterpret_cast<uint32_t *>(base + l.chunk_sums),
-            reinterpret_cast<uint32_t *>(base + l.slots), st);
+            reinterpret_cast<uint32_t *>(base + l.slots),
+            reinterpret_cast<uint32_t *>(base + l.counts), st);
         if (f != cudaErrorNotSupported) return cuda_code(f);
         (void)cudaGetLastError();  // not supported here: one launch per phase instead
     }

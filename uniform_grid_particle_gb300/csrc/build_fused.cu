@@ -3,16 +3,17 @@
 // The pages chain separate dispatches because the phases depend on each other
 // across workgroups ("Construir el índice de la rejilla…", §La cadena
 // completa: the scan needs every count, the scatter every start).  Here every
-// CTA of the grid is resident at once (cooperative launch, one or two CTAs
-// per SM), so a grid-wide barrier stands in for each kernel boundary:
+// CTA of the grid is resident at once (cooperative launch, two CTAs per SM),
+// so a grid-wide barrier stands in for each kernel boundary:
 //
-//   clear   conteos[0..C) = 0                              ("Poner a cero")
-//   count   celdaDe[i] = cell of particle i; the atomic that counts it
-//           returns its slot in the cell, kept in slots[i]  ("El kernel";
-//           the counter array is the cursor of "La dispersión")
-//   scan a  each CTA totals one contiguous chunk of conteos
-//   scan b  each CTA adds the totals of the chunks before it and scans its
-//           chunk into inicios; the last CTA writes inicios[C] = N
+//   count   celdaDe[i] = cell of particle i; the atomic that counts it in the
+//           workspace counter array returns its slot in the cell, kept in
+//           slots[i]  ("Contar partículas por celda", §El kernel; the counter
+//           array is also the cursor of "La dispersión")
+//   scan a  each CTA totals one contiguous chunk of the counters
+//   scan b  each CTA adds the totals of the chunks before it, scans its chunk
+//           into inicios, copies the counts to conteos and zeroes its
+//           counters; the last CTA writes inicios[C] = N
 //                                                     ("Del conteo al inicio")
 //   scatter ordenado[inicios[c] + slots[i]] = i        ("La dispersión")
 //   gather  destino[k] = origen[ordenado[k]]   ("El kernel de reordenación")
@@ -22,15 +23,25 @@
 // exactly as after their cursor scatter, and every output is one the pages'
 // chain can produce (order inside a cell is the atomics' arrival order).
 //
+// The counters live in the workspace and every build leaves them zero (scan b
+// zeroes them after reading), so no clear phase is needed ("Poner a cero" is
+// done by the previous build).  A header word records that they are clean; it
+// is dropped while a build is using them, so a build that did not finish
+// makes the next one clear them first.
+//
+// Particles (and the gather's half-records) are split into one contiguous,
+// equal range per CTA, so every CTA has the same work in every phase.
+//
 // The count reads each record's first 16 bytes with an L2 evict-last policy
 // and the gather reads the records with evict-first: the 32-byte sectors the
 // count brings into L2 are still there when the gather needs them.
 //
-// Grid barriers: every CTA adds one to a counter; the last one resets the
-// counter and bumps a generation word that the others poll with acquire
-// loads.  A wait gives up after kSpinLimitNs and records kStatusTimeout, so
-// the kernel cannot hang (co-residency is guaranteed by the cooperative
-// launch, so the limit is a guard, not part of the protocol).
+// Grid barriers: a CTA arrives with a release add on a counter that only grows
+// during the launch and waits, with acquire loads, until it reaches the number
+// of CTAs times the barriers passed; the last CTA to leave the kernel resets
+// it.  A wait gives up after kSpinLimitNs and records kStatusTimeout, so the
+// kernel cannot hang (co-residency is guaranteed by the cooperative launch, so
+// the limit is a guard, not part of the protocol).
 #include <atomic>
 
 #include "ugrid_internal.cuh"
@@ -71,10 +82,6 @@ __device__ __forceinline__ uint32_t load_acquire(const uint32_t *p) {
     return v;
 }
 
-__device__ __forceinline__ void store_release(uint32_t *p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ uint4 load_policy(const uint4 *p, unsigned long long policy) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
@@ -83,36 +90,31 @@ __device__ __forceinline__ uint4 load_policy(const uint4 *p, unsigned long long 
     return v;
 }
 
-__device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t *p) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
-    return old;
+__device__ __forceinline__ void arrive_release(uint32_t *p) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
 }
 
-// Thread 0 of every CTA carries `gen`, the barrier generation it waits past.
-// Arrival is a release (acq_rel) add, so the CTA's writes — made visible to
-// thread 0 by the __syncthreads — are published with it; the last CTA to
-// arrive has acquired every other arrival through the chain of adds, resets
-// the counter and publishes the new generation with a release store, which
-// the others read with acquire loads.
-__device__ void grid_barrier(grid_ws_header *hdr, uint32_t &gen) {
+// Thread 0 of every CTA counts the barriers it has passed in `passed`.  The
+// __syncthreads before the arrival makes the CTA's writes visible to thread 0,
+// whose release add publishes them; the acquire loads that see every arrival
+// make the other CTAs' writes visible, and the closing __syncthreads hands
+// them to the whole CTA.
+__device__ void grid_barrier(grid_ws_header *hdr, uint32_t &passed) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        const uint32_t target = gen + 1u;
-        if (arrive_acq_rel(&hdr->bar_count) == gridDim.x - 1u) {
-            hdr->bar_count = 0u;
-            store_release(&hdr->bar_gen, target);
-        } else {
+        passed += 1u;
+        const uint32_t target = passed * gridDim.x;
+        arrive_release(&hdr->bar_count);
+        if (load_acquire(&hdr->bar_count) < target) {
             const unsigned long long start = global_ns();
-            while (load_acquire(&hdr->bar_gen) != target) {
-                __nanosleep(20);
-                if (global_ns() - start > kSpinLimitNs) {
+            uint32_t polls = 0;
+            while (load_acquire(&hdr->bar_count) < target) {
+                if ((++polls & 31u) == 0 && global_ns() - start > kSpinLimitNs) {
                     record_status(&hdr->status, kStatusTimeout);
                     break;
                 }
             }
         }
-        gen = target;
     }
     __syncthreads();
 }
@@ -157,6 +159,45 @@ __device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s_red, uint32_t &
     return before + incl - v;
 }
 
+// Exclusive scans of kScanVecs rows at once: row q holds one value per
+// thread (t[q]); excl[q] receives the thread's exclusive prefix within row q
+// and rows[q] the row's total.  Two __syncthreads for all rows.
+__device__ __forceinline__ void rows_exclusive_scan(const uint32_t (&t)[kScanVecs],
+                                                    uint32_t (&excl)[kScanVecs],
+                                                    uint32_t (&rows)[kScanVecs],
+                                                    uint32_t (*s_rows)[kWarps]) {
+    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+    uint32_t incl[kScanVecs];
+#pragma unroll
+    for (int q = 0; q < kScanVecs; ++q) incl[q] = t[q];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int q = 0; q < kScanVecs; ++q) {
+            const uint32_t up = __shfl_up_sync(0xffffffffu, incl[q], o);
+            if (lane >= (uint32_t)o) incl[q] += up;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int q = 0; q < kScanVecs; ++q) s_rows[q][warp] = incl[q];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kScanVecs; ++q) {
+        uint32_t before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const uint32_t x = s_rows[q][w];
+            before += (uint32_t)w < warp ? x : 0u;
+            total += x;
+        }
+        excl[q] = before + incl[q] - t[q];
+        rows[q] = total;
+    }
+    __syncthreads();
+}
+
 // Four counts starting at cell c (a multiple of 4), zeros past `hi`.
 __device__ __forceinline__ uint4 load_counts(const uint32_t *conteos, uint64_t c, uint64_t hi) {
     if (c + 4 <= hi) return *reinterpret_cast<const uint4 *>(conteos + c);
@@ -180,49 +221,74 @@ __device__ __forceinline__ void store_starts(uint32_t *inicios, uint64_t c, uint
     }
 }
 
+// conteos[c..c+3] = v (the histogram) and counts[c..c+3] = 0 (only cells
+// below `hi`).
+__device__ __forceinline__ void store_counts(uint32_t *conteos, uint32_t *counts, uint64_t c, uint64_t hi,
+                                             const uint4 &v) {
+    if (c + 4 <= hi) {
+        *reinterpret_cast<uint4 *>(conteos + c) = v;
+        *reinterpret_cast<uint4 *>(counts + c) = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+        const uint32_t w[3] = {v.x, v.y, v.z};
+        for (int k = 0; k < 3; ++k) {
+            if (c + k < hi) {
+                conteos[c + k] = w[k];
+                counts[c + k] = 0u;
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
 build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino,
                    uint32_t *__restrict__ conteos, uint32_t *__restrict__ celdaDe,
                    uint32_t *__restrict__ inicios, uint32_t *__restrict__ ordenado, uint32_t n,
                    uint64_t cells, Geometry g, grid_ws_header *hdr, uint32_t *__restrict__ chunk_sums,
-                   uint32_t *__restrict__ slots) {
+                   uint32_t *__restrict__ slots, uint32_t *__restrict__ counts) {
     __shared__ uint32_t s_red[kWarps];
     __shared__ uint4 s_held[kScanVecs][kThreads];  // this CTA's chunk of counts (32 KB)
+    __shared__ uint32_t s_clean;
+    __shared__ uint32_t s_rows[kScanVecs][kWarps];
     const uint32_t tid = threadIdx.x;
     const uint32_t lane = tid & 31u;
-    const uint64_t grid_threads = (uint64_t)gridDim.x * kThreads;
-    uint32_t gen = 0;
-    if (tid == 0) gen = load_acquire(&hdr->bar_gen);  // before this CTA's first arrival
+    const uint32_t ctas = gridDim.x;
+    uint32_t passed = 0;  // grid barriers passed (thread 0)
+    // Read before this CTA's first arrival, hence before anyone changes it.
+    if (tid == 0) s_clean = *reinterpret_cast<volatile uint32_t *>(&hdr->counts_clean) >= cells;
+    __syncthreads();
+    // This CTA's particles: one contiguous, equal share.
+    const uint64_t p_lo = (uint64_t)n * blockIdx.x / ctas;
+    const uint64_t p_hi = (uint64_t)n * (blockIdx.x + 1) / ctas;
 
     UGRID_PHASE_MARK(0);
-    // ---- clear ---------------------------------------------------------------
-    {
+    // ---- clear the counters, only if the previous build did not leave them zero
+    if (!s_clean) {
         const uint64_t quads = cells / 4;
-        uint4 *c4 = reinterpret_cast<uint4 *>(conteos);
+        const uint64_t grid_threads = (uint64_t)ctas * kThreads;
+        uint4 *c4 = reinterpret_cast<uint4 *>(counts);
         for (uint64_t q = (uint64_t)blockIdx.x * kThreads + tid; q < quads; q += grid_threads)
             c4[q] = make_uint4(0u, 0u, 0u, 0u);
         for (uint64_t c = quads * 4 + (uint64_t)blockIdx.x * kThreads + tid; c < cells; c += grid_threads)
-            conteos[c] = 0u;
+            counts[c] = 0u;
+        grid_barrier(hdr, passed);
     }
-    UGRID_PHASE_END(0);
-    grid_barrier(hdr, gen);
 
     UGRID_PHASE_MARK(1);
     // ---- count: cell, histogram and slot -------------------------------------
     unsigned long long keep;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
-        for (uint64_t r0 = (uint64_t)blockIdx.x * kThreads * kCountItems; r0 < n; r0 += grid_threads * kCountItems) {
+    for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kCountItems) {
         uint4 rec[kCountItems];
 #pragma unroll
         for (int k = 0; k < kCountItems; ++k) {
             const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            if (i < n) rec[k] = load_policy(origen + 2 * i, keep);
+            if (i < p_hi) rec[k] = load_policy(origen + 2 * i, keep);
         }
         uint32_t cell[kCountItems], peers[kCountItems], base[kCountItems];
 #pragma unroll
         for (int k = 0; k < kCountItems; ++k) {
             const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            const bool valid = i < n;
+            const bool valid = i < p_hi;
             cell[k] = valid ? cell_of(rec[k], g) : 0u;
             if (valid) celdaDe[i] = cell[k];
             peers[k] = 1u << lane;
@@ -232,25 +298,27 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
             }
             base[k] = 0;
             if (valid && lane == (uint32_t)(__ffs(peers[k]) - 1))
-                base[k] = atomicAdd(conteos + cell[k], __popc(peers[k]));
+                base[k] = atomicAdd(counts + cell[k], __popc(peers[k]));
         }
 #pragma unroll
         for (int k = 0; k < kCountItems; ++k) {
             const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
             const uint32_t slot = __shfl_sync(0xffffffffu, base[k], __ffs(peers[k]) - 1) +
                                   __popc(peers[k] & lanemask_lt());
-            if (i < n) slots[i] = slot;
+            if (i < p_hi) slots[i] = slot;
         }
     }
     UGRID_PHASE_END(1);
-    grid_barrier(hdr, gen);
+    grid_barrier(hdr, passed);
+    // The counters are not zero until scan b has run to the end.
+    if (blockIdx.x == 0 && tid == 0) hdr->counts_clean = 0u;
 
     UGRID_PHASE_MARK(2);
     // ---- scan a: chunk totals --------------------------------------------------
     // Chunks are multiples of 4 cells so that 16-byte accesses stay aligned.
     // When a chunk fits in kScanVecs vectors per thread its counts stay in
     // shared memory for scan b; otherwise scan b reads them again.
-    const uint64_t chunk = ((cells + gridDim.x - 1) / gridDim.x + 3) & ~3ull;
+    const uint64_t chunk = ((cells + ctas - 1) / ctas + 3) & ~3ull;
     const uint64_t lo = min((uint64_t)blockIdx.x * chunk, cells);
     const uint64_t hi = min(lo + chunk, cells);
     const bool resident = chunk <= 4ull * kThreads * kScanVecs;
@@ -259,7 +327,7 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
         if (resident) {
             uint4 v[kScanVecs];
 #pragma unroll
-            for (int q = 0; q < kScanVecs; ++q) v[q] = load_counts(conteos, lo + 4ull * (q * kThreads + tid), hi);
+            for (int q = 0; q < kScanVecs; ++q) v[q] = load_counts(counts, lo + 4ull * (q * kThreads + tid), hi);
 #pragma unroll
             for (int q = 0; q < kScanVecs; ++q) {
                 s_held[q][tid] = v[q];
@@ -269,7 +337,7 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
             for (uint64_t c0 = lo; c0 < hi; c0 += 4ull * kThreads * kScanVecs) {
                 uint4 v[kScanVecs];
 #pragma unroll
-                for (int q = 0; q < kScanVecs; ++q) v[q] = load_counts(conteos, c0 + 4ull * (q * kThreads + tid), hi);
+                for (int q = 0; q < kScanVecs; ++q) v[q] = load_counts(counts, c0 + 4ull * (q * kThreads + tid), hi);
 #pragma unroll
                 for (int q = 0; q < kScanVecs; ++q) sum += v[q].x + v[q].y + v[q].z + v[q].w;
             }
@@ -278,41 +346,52 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
         if (tid == 0) chunk_sums[blockIdx.x] = sum;
     }
     UGRID_PHASE_END(2);
-    grid_barrier(hdr, gen);
+    grid_barrier(hdr, passed);
 
     UGRID_PHASE_MARK(3);
-    // ---- scan b: exclusive scan of this chunk, offset by the earlier chunks ---
+    // ---- scan b: starts, histogram copy, counters back to zero ---------------
     {
         uint32_t before = 0;
         for (uint32_t b = tid; b < blockIdx.x; b += kThreads) before += chunk_sums[b];
         uint32_t prefix = block_sum(before, s_red);
         for (uint64_t c0 = lo; c0 < hi; c0 += 4ull * kThreads * kScanVecs) {
             uint4 v[kScanVecs];
-#pragma unroll
-            for (int q = 0; q < kScanVecs; ++q)
-                v[q] = resident ? s_held[q][tid] : load_counts(conteos, c0 + 4ull * (q * kThreads + tid), hi);
+            uint32_t t[kScanVecs];
 #pragma unroll
             for (int q = 0; q < kScanVecs; ++q) {
-                uint32_t total;
-                const uint32_t excl = block_exclusive_scan(v[q].x + v[q].y + v[q].z + v[q].w, s_red, total);
-                store_starts(inicios, c0 + 4ull * (q * kThreads + tid), hi, prefix + excl, v[q]);
-                prefix += total;
+                v[q] = resident ? s_held[q][tid] : load_counts(counts, c0 + 4ull * (q * kThreads + tid), hi);
+                t[q] = v[q].x + v[q].y + v[q].z + v[q].w;
             }
+            // All kScanVecs rows at once: warp scans, then one exchange of the
+            // warp totals through shared memory.
+            uint32_t excl[kScanVecs], rows[kScanVecs];
+            rows_exclusive_scan(t, excl, rows, s_rows);
+            uint32_t row_base = prefix;
+#pragma unroll
+            for (int q = 0; q < kScanVecs; ++q) {
+                const uint64_t c = c0 + 4ull * (q * kThreads + tid);
+                store_starts(inicios, c, hi, row_base + excl[q], v[q]);
+                store_counts(conteos, counts, c, hi, v[q]);
+                row_base += rows[q];
+            }
+            prefix = row_base;
         }
-        if (blockIdx.x == gridDim.x - 1 && tid == 0) inicios[cells] = prefix;
+        if (blockIdx.x == ctas - 1 && tid == 0) inicios[cells] = prefix;
     }
     UGRID_PHASE_END(3);
-    grid_barrier(hdr, gen);
+    grid_barrier(hdr, passed);
+    // Every CTA zeroed its counters before that barrier.
+    if (blockIdx.x == 0 && tid == 0 && (hdr->status & kStatusTimeout) == 0)
+        hdr->counts_clean = (uint32_t)cells;
 
     UGRID_PHASE_MARK(4);
     // ---- scatter: every particle to its slot ----------------------------------
-    for (uint64_t r0 = (uint64_t)blockIdx.x * kThreads * kScatterItems; r0 < n;
-         r0 += grid_threads * kScatterItems) {
+    for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
         uint32_t cell[kScatterItems], slot[kScatterItems], start[kScatterItems];
 #pragma unroll
         for (int k = 0; k < kScatterItems; ++k) {
             const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            if (i < n) {
+            if (i < p_hi) {
                 cell[k] = celdaDe[i];
                 slot[k] = slots[i];
             }
@@ -320,12 +399,12 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
 #pragma unroll
         for (int k = 0; k < kScatterItems; ++k) {
             const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            if (i < n) start[k] = inicios[cell[k]];
+            if (i < p_hi) start[k] = inicios[cell[k]];
         }
 #pragma unroll
         for (int k = 0; k < kScatterItems; ++k) {
             const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            if (i < n) {
+            if (i < p_hi) {
                 const uint32_t pos = start[k] + slot[k];
                 if (pos < n)
                     ordenado[pos] = (uint32_t)i;
@@ -335,30 +414,30 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
         }
     }
     UGRID_PHASE_END(4);
-    grid_barrier(hdr, gen);
+    grid_barrier(hdr, passed);
 
     UGRID_PHASE_MARK(5);
     // ---- gather: two threads per 32-byte record -------------------------------
     unsigned long long last_use;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(last_use));
-    const uint64_t halves = 2ull * n;
-    for (uint64_t r0 = (uint64_t)blockIdx.x * kThreads * kGatherItems; r0 < halves; r0 += grid_threads * kGatherItems) {
+    const uint64_t h_lo = 2 * p_lo, h_hi = 2 * p_hi;
+    for (uint64_t r0 = h_lo; r0 < h_hi; r0 += (uint64_t)kThreads * kGatherItems) {
         uint32_t src[kGatherItems];
 #pragma unroll
         for (int k = 0; k < kGatherItems; ++k) {
             const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
-            src[k] = h < halves ? ordenado[h >> 1] : 0u;
+            src[k] = h < h_hi ? ordenado[h >> 1] : 0u;
         }
         uint4 v[kGatherItems];
 #pragma unroll
         for (int k = 0; k < kGatherItems; ++k) {
             const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
-            if (h < halves && src[k] < n) v[k] = load_policy(origen + 2 * (uint64_t)src[k] + (h & 1), last_use);
+            if (h < h_hi && src[k] < n) v[k] = load_policy(origen + 2 * (uint64_t)src[k] + (h & 1), last_use);
         }
 #pragma unroll
         for (int k = 0; k < kGatherItems; ++k) {
             const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
-            if (h < halves) {
+            if (h < h_hi) {
                 if (src[k] < n)
                     store_cs(destino + h, v[k]);
                 else if ((h & 1) == 0)
@@ -367,6 +446,12 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
         }
     }
     UGRID_PHASE_MARK(6);
+
+    // The last CTA out resets the barrier counter for the next launch.
+    if (tid == 0 && atomicAdd(&hdr->bar_exit, 1u) == ctas - 1u) {
+        hdr->bar_count = 0u;
+        hdr->bar_exit = 0u;
+    }
 }
 
 std::atomic<int> g_grid[kMaxDevices];  // cached grid size per device (0 = not yet known)
@@ -399,7 +484,7 @@ cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *d
                                uint32_t *conteos, uint32_t *celdaDe, uint32_t *inicios,
                                uint32_t *ordenado, uint32_t n, uint64_t cells, const Geometry &g,
                                grid_ws_header *hdr, uint32_t *chunk_sums, uint32_t *slots,
-                               cudaStream_t s) {
+                               uint32_t *counts, cudaStream_t s) {
     int device = 0, grid = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e == cudaSuccess) e = fused_grid(device, &grid);
@@ -416,7 +501,7 @@ cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *d
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, build_fused_kernel, reinterpret_cast<const uint4 *>(origen),
                               reinterpret_cast<uint4 *>(destino), conteos, celdaDe, inicios, ordenado,
-                              n, cells, g, hdr, chunk_sums, slots);
+                              n, cells, g, hdr, chunk_sums, slots, counts);
 }
 
 }  // namespace ugrid

@@ -38,6 +38,7 @@ struct WsLayout {
     size_t tile_status;     // u64[tiles]
     size_t chunk_sums;      // u32[kFusedMaxCtas] per-CTA cell-chunk totals (fused build)
     size_t slots;           // u32[n] slot of each particle in its cell (fused build)
+    size_t counts;          // u32[cells] counters of the fused build, zero between builds
     size_t stable_queue;    // u32[cells] queue of long segments (GRID_STABLE)
     size_t stable_scratch;  // u32[n] radix-sort scratch (GRID_STABLE)
     size_t total;
@@ -90,7 +91,7 @@ cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *d
                                uint32_t *conteos, uint32_t *celdaDe, uint32_t *inicios,
                                uint32_t *ordenado, uint32_t n, uint64_t cells, const Geometry &g,
                                grid_ws_header *hdr, uint32_t *chunk_sums, uint32_t *slots,
-                               cudaStream_t s);
+                               uint32_t *counts, cudaStream_t s);
 
 // Queue entries needed for cells longer than the register tier (<= cells).
 size_t segment_queue_capacity(uint64_t n, uint64_t cells);
