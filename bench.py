@@ -159,6 +159,12 @@ def max_over_ranks(value: float, dist) -> float:
     return float(t.item())
 
 
+def job_rate(world: int, n_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job Mparticles/s: every rank builds n_per_rank particles per step and
+    the step lasts as long as the slowest rank's (ms_per_step is that maximum)."""
+    return world * n_per_rank / (ms_per_step / 1e3) / 1e6
+
+
 def barrier(dist) -> None:
     if dist is not None:
         dist.barrier()
@@ -321,7 +327,7 @@ def run_gpu(args) -> None:
     check_status("the timed steps")
     total_ms = max_over_ranks(sum(step_ms), dist)
     ms_per_step = total_ms / args.steps
-    value = world * n / (ms_per_step / 1e3) / 1e6
+    value = job_rate(world, n, ms_per_step)
     kernels_per_step = 1 if not args.stable else 6   # the fused kernel; the stable chain launches six
 
     # ---- the same build replayed from a CUDA graph ----
@@ -387,7 +393,7 @@ def run_gpu(args) -> None:
     e2e_ms = timed(e2e_step, args.e2e_steps)
     check_status("the end-to-end pass")
     e2e_total = max_over_ranks(sum(e2e_ms), dist)
-    e2e_value = world * n / (e2e_total / len(e2e_ms) / 1e3) / 1e6
+    e2e_value = job_rate(world, n, e2e_total / len(e2e_ms))
     if not np.array_equal(host_inicios.numpy()[[0, cells]], np.array([0, n], dtype=np.int32)):
         raise RuntimeError("end-to-end result is inconsistent")
 
