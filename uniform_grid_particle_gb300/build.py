@@ -20,7 +20,8 @@ LIBRARY = os.path.join(PKG, "libugrid.so")
 
 SOURCES = ["abi.cu", "build_fused.cu", "count.cu", "scan.cu", "scatter.cu", "reorder.cu", "segsort.cu",
            "scan_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "ugrid_internal.cuh"), os.path.join(INCLUDE, "ugrid.h")]
+HEADERS = [os.path.join(CSRC, "ugrid_internal.cuh"), os.path.join(CSRC, "segsort_device.cuh"),
+           os.path.join(INCLUDE, "ugrid.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

@@ -1,4 +1,4 @@
-// The whole (non-stable) grid build in one cooperative launch.
+// The whole grid build in one cooperative launch.
 //
 // The pages chain separate dispatches because the phases depend on each other
 // across workgroups ("Construir el índice de la rejilla…", §La cadena
@@ -29,6 +29,11 @@
 // is dropped while a build is using them, so a build that did not finish
 // makes the next one clear them first.
 //
+// With GRID_STABLE two phases follow the scatter: one thread per cell sorts
+// its segment in registers when it holds at most 32 particles and queues it
+// otherwise, then CTAs take the queued segments one each (bitonic in shared
+// memory up to 8192, an LSD radix sort through the workspace beyond).
+//
 // Particles (and the gather's half-records) are split into one contiguous,
 // equal range per CTA, so every CTA has the same work in every phase.
 //
@@ -44,7 +49,7 @@
 // the limit is a guard, not part of the protocol).
 #include <atomic>
 
-#include "ugrid_internal.cuh"
+#include "segsort_device.cuh"
 
 namespace ugrid {
 namespace {
@@ -239,12 +244,25 @@ __device__ __forceinline__ void store_counts(uint32_t *conteos, uint32_t *counts
     }
 }
 
+// Workspace arrays of the fused build.
+struct FusedScratch {
+    uint32_t *chunk_sums;      // per-CTA chunk totals
+    uint32_t *slots;           // per-particle slot in its cell
+    uint32_t *counts;          // per-cell counters, zero between builds
+    uint32_t *queue;           // stable mode: cells longer than kRegisterMax
+    uint32_t queue_capacity;
+    uint32_t *sort_scratch;    // stable mode: radix ping-pong buffer (N words)
+};
+
+template <bool kStable>
 __global__ void __launch_bounds__(kThreads, 2)
 build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino,
                    uint32_t *__restrict__ conteos, uint32_t *__restrict__ celdaDe,
                    uint32_t *__restrict__ inicios, uint32_t *__restrict__ ordenado, uint32_t n,
-                   uint64_t cells, Geometry g, grid_ws_header *hdr, uint32_t *__restrict__ chunk_sums,
-                   uint32_t *__restrict__ slots, uint32_t *__restrict__ counts) {
+                   uint64_t cells, Geometry g, grid_ws_header *hdr, FusedScratch ws) {
+    uint32_t *__restrict__ chunk_sums = ws.chunk_sums;
+    uint32_t *__restrict__ slots = ws.slots;
+    uint32_t *__restrict__ counts = ws.counts;
     __shared__ uint32_t s_red[kWarps];
     __shared__ uint4 s_held[kScanVecs][kThreads];  // this CTA's chunk of counts (32 KB)
     __shared__ uint32_t s_clean;
@@ -255,6 +273,8 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
     uint32_t passed = 0;  // grid barriers passed (thread 0)
     // Read before this CTA's first arrival, hence before anyone changes it.
     if (tid == 0) s_clean = *reinterpret_cast<volatile uint32_t *>(&hdr->counts_clean) >= cells;
+    // Nobody touches the long-segment queue before the stable phases.
+    if (kStable && blockIdx.x == 0 && tid == 0) hdr->stable_big = 0u;
     __syncthreads();
     // This CTA's particles: one contiguous, equal share.
     const uint64_t p_lo = (uint64_t)n * blockIdx.x / ctas;
@@ -416,6 +436,36 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
     UGRID_PHASE_END(4);
     grid_barrier(hdr, passed);
 
+    if (kStable) {
+        // ---- stable mode: every cell's segment sorted by particle index ------
+        // ("Construir el índice…", §El orden dentro de la celda.)  Short
+        // segments are sorted by one thread in registers; longer ones are queued.
+        const uint64_t grid_threads = (uint64_t)ctas * kThreads;
+        for (uint64_t c = (uint64_t)blockIdx.x * kThreads + tid; c < cells; c += grid_threads) {
+            const uint32_t a = inicios[c];
+            if (!sort_short_segment(ordenado + a, inicios[c + 1] - a)) {
+                const uint32_t q = atomicAdd(&hdr->stable_big, 1u);
+                if (q < ws.queue_capacity)
+                    ws.queue[q] = (uint32_t)c;
+                else
+                    record_status(&hdr->status, kStatusBounds);
+            }
+        }
+        grid_barrier(hdr, passed);
+        // Long segments, one CTA each: bitonic in shared memory up to 8192
+        // indices, radix through the workspace scratch beyond.
+        const uint32_t queued = *reinterpret_cast<volatile uint32_t *>(&hdr->stable_big);
+        const uint32_t count = min(queued, ws.queue_capacity);
+        uint32_t *s_buf = reinterpret_cast<uint32_t *>(&s_held[0][0]);
+        for (uint32_t q = blockIdx.x; q < count; q += ctas) {
+            const uint32_t c = ws.queue[q];
+            const uint32_t a = inicios[c];
+            sort_long_segment<kThreads>(ordenado + a, ws.sort_scratch + a, inicios[c + 1] - a, n, s_buf,
+                                        kScanVecs * kThreads * 4);
+        }
+        grid_barrier(hdr, passed);
+    }
+
     UGRID_PHASE_MARK(5);
     // ---- gather: two threads per 32-byte record -------------------------------
     unsigned long long last_use;
@@ -468,7 +518,7 @@ cudaError_t fused_grid(int device, int *grid) {
     cudaError_t e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_fused_kernel, kThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_fused_kernel<true>, kThreads, 0);
     if (e != cudaSuccess) return e;
     int g = coop ? per_sm * sms : -1;
     if (g == 0) g = -1;
@@ -484,7 +534,8 @@ cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *d
                                uint32_t *conteos, uint32_t *celdaDe, uint32_t *inicios,
                                uint32_t *ordenado, uint32_t n, uint64_t cells, const Geometry &g,
                                grid_ws_header *hdr, uint32_t *chunk_sums, uint32_t *slots,
-                               uint32_t *counts, cudaStream_t s) {
+                               uint32_t *counts, bool stable, uint32_t *queue,
+                               uint32_t queue_capacity, uint32_t *sort_scratch, cudaStream_t s) {
     int device = 0, grid = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e == cudaSuccess) e = fused_grid(device, &grid);
@@ -499,9 +550,10 @@ cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *d
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, build_fused_kernel, reinterpret_cast<const uint4 *>(origen),
-                              reinterpret_cast<uint4 *>(destino), conteos, celdaDe, inicios, ordenado,
-                              n, cells, g, hdr, chunk_sums, slots, counts);
+    const FusedScratch ws{chunk_sums, slots, counts, queue, queue_capacity, sort_scratch};
+    return cudaLaunchKernelEx(&cfg, stable ? build_fused_kernel<true> : build_fused_kernel<false>,
+                              reinterpret_cast<const uint4 *>(origen), reinterpret_cast<uint4 *>(destino),
+                              conteos, celdaDe, inicios, ordenado, n, cells, g, hdr, ws);
 }
 
 }  // namespace ugrid

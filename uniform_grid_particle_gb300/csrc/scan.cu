@@ -76,20 +76,32 @@ __device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t ti
             const long long idx = j - (long long)(w * 32 + lane);
             s[w] = idx >= 0 ? load_relaxed(tile_status + idx) : kFlagPrefix;
         }
+        // Wait until every word of the window is published, re-reading all the
+        // pending ones together (one round trip per poll, not one per word).
+        bool pending = false;
 #pragma unroll
-        for (int w = 0; w < kLookWords; ++w) {
-            if ((s[w] >> 32) == 0) {
-                const long long idx = j - (long long)(w * 32 + lane);
-                const unsigned long long start = global_ns();
-                do {
-                    __nanosleep(64);
-                    s[w] = load_relaxed(tile_status + idx);
-                    if ((s[w] >> 32) == 0 && global_ns() - start > kSpinLimitNs) {
-                        record_status(status_word, kStatusTimeout);
-                        s[w] = kFlagPrefix;  // give up: carry on with a zero prefix
+        for (int w = 0; w < kLookWords; ++w) pending |= (s[w] >> 32) == 0;
+        if (__any_sync(kFullMask, pending)) {
+            const unsigned long long start = global_ns();
+            do {
+                __nanosleep(32);
+                pending = false;
+#pragma unroll
+                for (int w = 0; w < kLookWords; ++w) {
+                    if ((s[w] >> 32) == 0) {
+                        s[w] = load_relaxed(tile_status + (j - (long long)(w * 32 + lane)));
+                        pending |= (s[w] >> 32) == 0;
                     }
-                } while ((s[w] >> 32) == 0);
-            }
+                }
+                const bool give_up = __shfl_sync(kFullMask, global_ns() - start > kSpinLimitNs, 0);
+                if (give_up && __any_sync(kFullMask, pending)) {
+#pragma unroll
+                    for (int w = 0; w < kLookWords; ++w)
+                        if ((s[w] >> 32) == 0) s[w] = kFlagPrefix;  // carry on with a zero prefix
+                    if (lane == 0) record_status(status_word, kStatusTimeout);
+                    pending = false;
+                }
+            } while (__any_sync(kFullMask, pending));
         }
         // Position (w*32 + lane) of the nearest inclusive prefix in the window.
         uint32_t nearest = 0xffffffffu;

@@ -84,14 +84,15 @@ cudaError_t launch_reorder(const uint32_t *ordenado, const ugrid_particula *orig
                            ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s,
                            bool pdl);
 
-// The whole non-stable build in one cooperative launch (see build_fused.cu).
+// The whole build in one cooperative launch (see build_fused.cu).
 // Returns cudaErrorNotSupported when the device cannot run it, so the caller
 // can fall back to one launch per phase.
 cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *destino,
                                uint32_t *conteos, uint32_t *celdaDe, uint32_t *inicios,
                                uint32_t *ordenado, uint32_t n, uint64_t cells, const Geometry &g,
                                grid_ws_header *hdr, uint32_t *chunk_sums, uint32_t *slots,
-                               uint32_t *counts, cudaStream_t s);
+                               uint32_t *counts, bool stable, uint32_t *queue,
+                               uint32_t queue_capacity, uint32_t *sort_scratch, cudaStream_t s);
 
 // Queue entries needed for cells longer than the register tier (<= cells).
 size_t segment_queue_capacity(uint64_t n, uint64_t cells);
