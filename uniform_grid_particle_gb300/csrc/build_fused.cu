@@ -9,7 +9,9 @@
 //   count   celdaDe[i] = cell of particle i; the atomic that counts it in the
 //           workspace counter array returns its slot in the cell, kept in
 //           slots[i]  ("Contar partículas por celda", §El kernel; the counter
-//           array is also the cursor of "La dispersión")
+//           array is also the cursor of "La dispersión").  Particles of one
+//           CTA that share a cell are grouped first and take their slots with
+//           one atomic (§La contención de las celdas densas)
 //   scan a  each CTA totals one contiguous chunk of the counters
 //   scan b  each CTA adds the totals of the chunks before it, scans its chunk
 //           into inicios, copies the counts to conteos and zeroes its
@@ -79,6 +81,11 @@ constexpr int kCountItems = UGRID_FUSED_COUNT_ITEMS;      // particles per threa
 constexpr int kScatterItems = UGRID_FUSED_SCATTER_ITEMS;  // particles per thread per round
 constexpr int kGatherItems = UGRID_FUSED_GATHER_ITEMS;    // half-records per thread per round
 constexpr int kScanVecs = 4;  // 16-byte vectors of counts a thread keeps between the scan phases
+constexpr int kAggBits = 11;  // the count's per-CTA grouping table: 2^11 entries
+constexpr int kAggSlots = 1 << kAggBits;
+constexpr uint32_t kAggEmpty = 0xffffffffu;  // never a cell index (cells < 2^32 - 1)
+static_assert(kAggSlots % kThreads == 0 && 2 * kAggSlots <= kScanVecs * kThreads * 4,
+              "grouping table must fit in s_held");
 constexpr int kMaxDevices = 64;
 
 __device__ __forceinline__ uint32_t load_acquire(const uint32_t *p) {
@@ -297,6 +304,15 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
     // ---- count: cell, histogram and slot -------------------------------------
     unsigned long long keep;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+    // Each round the CTA groups its particles by cell in a shared-memory hash
+    // table (the counts' s_held space is free until scan a): the particles of a
+    // cell that claims an entry take their slots with one global atomic for the
+    // whole group, so a crowded cell costs one atomic per CTA and round rather
+    // than one per particle ("Contar partículas por celda", §La contención de
+    // las celdas densas: aggregate, then one contribution per group).  A
+    // particle whose entry another cell holds takes its slot directly.
+    uint32_t *s_key = reinterpret_cast<uint32_t *>(&s_held[0][0]);  // [kAggSlots] cell or kAggEmpty
+    uint32_t *s_cnt = s_key + kAggSlots;                              // [kAggSlots] count, then base
     for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kCountItems) {
         uint4 rec[kCountItems];
 #pragma unroll
@@ -304,29 +320,47 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
             const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
             if (i < p_hi) rec[k] = load_policy(origen + 2 * i, keep);
         }
-        uint32_t cell[kCountItems], peers[kCountItems], base[kCountItems];
+#pragma unroll
+        for (int e = 0; e < kAggSlots / kThreads; ++e) {
+            s_key[e * kThreads + tid] = kAggEmpty;
+            s_cnt[e * kThreads + tid] = 0u;
+        }
+        __syncthreads();
+        uint32_t entry[kCountItems], rank[kCountItems];
 #pragma unroll
         for (int k = 0; k < kCountItems; ++k) {
             const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            const bool valid = i < p_hi;
-            cell[k] = valid ? cell_of(rec[k], g) : 0u;
-            if (valid) celdaDe[i] = cell[k];
-            peers[k] = 1u << lane;
-            if (warp_has_adjacent_duplicates(valid, cell[k])) {
-                const uint32_t active = __ballot_sync(0xffffffffu, valid);
-                if (valid) peers[k] = __match_any_sync(active, cell[k]);
+            entry[k] = kAggEmpty;
+            if (i < p_hi) {
+                const uint32_t c = cell_of(rec[k], g);
+                celdaDe[i] = c;
+                const uint32_t h = (c * 0x9E3779B1u) >> (32 - kAggBits);
+                const uint32_t held = atomicCAS(&s_key[h], kAggEmpty, c);
+                if (held == kAggEmpty || held == c) {
+                    entry[k] = h;
+                    rank[k] = atomicAdd(&s_cnt[h], 1u);
+                } else {
+                    rank[k] = atomicAdd(counts + c, 1u);
+                }
             }
-            base[k] = 0;
-            if (valid && lane == (uint32_t)(__ffs(peers[k]) - 1))
-                base[k] = atomicAdd(counts + cell[k], __popc(peers[k]));
         }
+        __syncthreads();
+        // One atomic per claimed entry; the entry's count becomes its base slot.
+        uint32_t group[kAggSlots / kThreads];
+#pragma unroll
+        for (int e = 0; e < kAggSlots / kThreads; ++e) {
+            const uint32_t m = s_cnt[e * kThreads + tid];
+            group[e] = m ? atomicAdd(counts + s_key[e * kThreads + tid], m) : 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < kAggSlots / kThreads; ++e) s_cnt[e * kThreads + tid] = group[e];
+        __syncthreads();
 #pragma unroll
         for (int k = 0; k < kCountItems; ++k) {
             const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            const uint32_t slot = __shfl_sync(0xffffffffu, base[k], __ffs(peers[k]) - 1) +
-                                  __popc(peers[k] & lanemask_lt());
-            if (i < p_hi) slots[i] = slot;
+            if (i < p_hi) slots[i] = entry[k] == kAggEmpty ? rank[k] : s_cnt[entry[k]] + rank[k];
         }
+        __syncthreads();  // the table is cleared at the top of the next round
     }
     UGRID_PHASE_END(1);
     grid_barrier(hdr, passed);
