@@ -195,6 +195,38 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
 int grid_scan_noalloc(const uint32_t *conteos, uint32_t *inicios, const grid_params *p,
                       void *stream);
 
+/* One particle array for grid_reorder_many: device pointers to N records of
+ * record_bytes bytes each (a multiple of 16, at most 256), 16-byte aligned. */
+typedef struct grid_array {
+    const void *origen;
+    void *destino;
+    uint32_t record_bytes;
+} grid_array;
+
+/* Gather several arrays with one ordenado ("Reordenar por celda…", §El kernel
+ * de reordenación: when the state lives in several buffers, one kernel that
+ * reads ordenado[k] once for all of them beats one kernel per buffer; "El
+ * estado de las partículas…", §AoS o SoA: the hot/cold split).  For every
+ * array a and k < N: destino_a[k] = origen_a[ordenado[k]].
+ * arrays: host array of `count` descriptors, 1 <= count <= 4.  Every destino
+ * must be distinct from every origen and destino, ordenado and the workspace
+ * header.  An index >= N sets status bit 1 (see grid_status) and that record
+ * is not written. */
+int grid_reorder_many(const uint32_t *ordenado, const grid_array *arrays, uint32_t count, void *ws,
+                      const grid_params *p, void *stream);
+
+/* Overflow diagnostics ("Contar partículas por celda", §Detectar el
+ * desbordamiento sin salir de la GPU): for a per-cell capacity, the largest
+ * occupancy (maxPorCelda: the page's atomicMax of previo + 1 while counting)
+ * and the number of particles that arrived over the capacity (desbordes).
+ * Both are fixed by the histogram, so they are computed from it in one pass:
+ *   diag[0] = max_c conteos[c],  diag[1] = sum_c max(0, conteos[c] - capacidad).
+ * conteos: u32[C] (read), 16-byte aligned, e.g. as left by grid_count or
+ * grid_build.  diag: u32[2] device array (written; zeroed first on `stream`).
+ * The page uses capacidad = 64. */
+int grid_diagnostics(const uint32_t *conteos, uint32_t capacidad, uint32_t *diag,
+                     const grid_params *p, void *stream);
+
 /* Synchronise `stream`, read and clear the workspace status word, and return
  * GRID_OK, GRID_ETIMEOUT (bit 0 set) or GRID_EBOUNDS (bit 1 set); GRID_ECUDA
  * if the copy or the synchronisation failed. */

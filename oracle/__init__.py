@@ -57,8 +57,11 @@ class Oracle:
         lib.oracle_build.argtypes = [_f32p, u64, _u32p, _f32p, ctypes.c_float,
                                      _u32p, _u32p, _u32p, _u32p, _f32p]
         lib.oracle_canonicalise.argtypes = [_u32p, u64, _u32p]
+        lib.oracle_diagnostics.argtypes = [_u32p, u64, u64, ctypes.c_uint32, _u32p, _u32p]
+        lib.oracle_reorder_records.argtypes = [_u32p, u64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32]
         for f in ("oracle_cell_index", "oracle_histogram", "oracle_exclusive_scan",
-                  "oracle_scatter", "oracle_reorder", "oracle_build", "oracle_canonicalise"):
+                  "oracle_scatter", "oracle_reorder", "oracle_build", "oracle_canonicalise",
+                  "oracle_diagnostics", "oracle_reorder_records"):
             getattr(lib, f).restype = None
         self.lib = lib
 
@@ -104,6 +107,18 @@ class Oracle:
                                 out.ctypes.data_as(ctypes.c_void_p))
         return out
 
+    def reorder_records(self, ordenado, origen: np.ndarray) -> np.ndarray:
+        """destino[k] = origen[ordenado[k]] for one array of equal-size records
+        (origen: [N, record_bytes] uint8, or any array whose rows are the records)."""
+        ordenado = np.ascontiguousarray(ordenado, dtype=np.uint32)
+        src = np.ascontiguousarray(origen)
+        rb = src.nbytes // max(src.shape[0], 1) if src.shape[0] else 0
+        out = np.empty((ordenado.size,) + src.shape[1:], dtype=src.dtype)
+        self.lib.oracle_reorder_records(_ptr(ordenado, _u32p), ordenado.size,
+                                        src.ctypes.data_as(ctypes.c_void_p),
+                                        out.ctypes.data_as(ctypes.c_void_p), rb)
+        return out
+
     def build(self, parts, dims, origin, cell_size) -> dict:
         """The whole chain; returns conteos, celdaDe, inicios, ordenado, destino."""
         parts = np.ascontiguousarray(parts, dtype=np.float32).reshape(-1, 8)
@@ -123,6 +138,15 @@ class Oracle:
                               _ptr(out["celdaDe"], _u32p), _ptr(out["inicios"], _u32p),
                               _ptr(out["ordenado"], _u32p), _ptr(out["destino"], _f32p))
         return out
+
+    def diagnostics(self, celda_de, cells: int, capacidad: int = 64) -> tuple[int, int]:
+        """(maxPorCelda, desbordes) while counting the particles in index order."""
+        celda_de = np.ascontiguousarray(celda_de, dtype=np.uint32)
+        cursor = np.empty(max(cells, 1), dtype=np.uint32)
+        diag = np.zeros(2, dtype=np.uint32)
+        self.lib.oracle_diagnostics(_ptr(celda_de, _u32p), celda_de.size, cells, capacidad,
+                                    _ptr(cursor, _u32p), _ptr(diag, _u32p))
+        return int(diag[0]), int(diag[1])
 
     def canonicalise(self, inicios, ordenado) -> np.ndarray:
         """Copy of ordenado with every cell segment sorted ascending."""

@@ -149,3 +149,37 @@ void oracle_canonicalise(const uint32_t *inicios, uint64_t cells, uint32_t *orde
             qsort(ordenado + a, b - a, sizeof(uint32_t), cmp_u32);
     }
 }
+
+/* [count] §Detectar el desbordamiento sin salir de la GPU: while counting,
+ * previo is the counter before this particle, so previo + 1 is the cell's
+ * occupancy after it; maxPorCelda keeps the largest occupancy seen and
+ * desbordes counts the particles that arrive when it exceeds capacidad.
+ * diag[0] = maxPorCelda, diag[1] = desbordes. */
+void oracle_diagnostics(const uint32_t *celdaDe, uint64_t n, uint64_t cells, uint32_t capacidad,
+                        uint32_t *cursor, uint32_t diag[2])
+{
+    memset(cursor, 0, cells * sizeof(uint32_t));
+    diag[0] = 0u;
+    diag[1] = 0u;
+    for (uint64_t i = 0; i < n; ++i) {
+        uint32_t previo = cursor[celdaDe[i]];
+        cursor[celdaDe[i]] = previo + 1u;
+        if (previo + 1u > diag[0])
+            diag[0] = previo + 1u;
+        if (previo + 1u > capacidad)
+            diag[1] += 1u;
+    }
+}
+
+/* [reorder] §El kernel de reordenación, state in several buffers: the same
+ * ordenado applied to every buffer.  For one buffer of record_bytes-byte
+ * records: destino[k] = origen[ordenado[k]]; the caller applies it to each
+ * buffer in turn. */
+void oracle_reorder_records(const uint32_t *ordenado, uint64_t n, const void *origen, void *destino,
+                            uint32_t record_bytes)
+{
+    const unsigned char *src = (const unsigned char *)origen;
+    unsigned char *dst = (unsigned char *)destino;
+    for (uint64_t k = 0; k < n; ++k)
+        memcpy(dst + (uint64_t)record_bytes * k, src + (uint64_t)record_bytes * ordenado[k], record_bytes);
+}

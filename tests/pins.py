@@ -264,6 +264,39 @@ def pin_canonicalise(o, seed: int = 9) -> None:
     assert np.array_equal(o.canonicalise(inicios, shuffled), stable)
 
 
+def pin_reorder_records(o, seed: int = 13) -> None:
+    """Any record size: numpy fancy indexing; 32-byte records: the same as the
+    particle gather."""
+    rng = np.random.default_rng(seed)
+    for n in (0, 1, 777):
+        perm = rng.permutation(n).astype(np.uint32)
+        for rb in (16, 32, 48, 256):
+            recs = rng.integers(0, 256, (n, rb), dtype=np.uint8)
+            assert np.array_equal(o.reorder_records(perm, recs), recs[perm]), f"record size {rb}"
+        parts = rng.random((n, 8), dtype=np.float32)
+        assert np.array_equal(o.reorder_records(perm, parts), o.reorder(perm, parts))
+
+
+# ---------------------------------------------------------------- diagnostics
+
+def pin_diagnostics(o, seed: int = 12) -> None:
+    """Hand-evaluated cases, then the closed forms maxPorCelda = max(conteos)
+    and desbordes = sum over cells of max(0, conteos - capacidad)."""
+    for row in read_golden("overflow_diagnostics.txt"):
+        text = " ".join(row)
+        cap_s, cells_s, want_s = [part.strip() for part in text.split(";")]
+        celda = np.array([int(v) for v in cells_s.split()], dtype=np.uint32)
+        want = tuple(int(v) for v in want_s.split())
+        cells = int(celda.max()) + 1 if celda.size else 1
+        assert o.diagnostics(celda, cells, int(cap_s)) == want, f"{text}"
+    rng = np.random.default_rng(seed)
+    for n, cells, cap in ((5000, 40, 64), (20000, 100, 150), (3000, 5000, 1), (0, 7, 64)):
+        celda = rng.integers(0, cells, n, dtype=np.uint32)
+        counts = np.bincount(celda, minlength=cells).astype(np.int64)
+        want = (int(counts.max()) if n else 0, int(np.maximum(counts - cap, 0).sum()))
+        assert o.diagnostics(celda, cells, cap) == want
+
+
 ALL_PINS = [
     pin_cell_index_special_positions,
     pin_linear_index_table,
@@ -276,6 +309,8 @@ ALL_PINS = [
     pin_build_degenerate,
     pin_build_brute_force,
     pin_canonicalise,
+    pin_diagnostics,
+    pin_reorder_records,
 ]
 
 

@@ -152,3 +152,28 @@ def test_binding_checks_tensors_before_the_library(L):
     p = P(L, 10)
     with pytest.raises(ValueError):
         L.grid_clear(torch.zeros(4096, dtype=torch.int32), p)          # CPU tensor
+
+
+def test_reorder_many_and_diagnostics_validation(L):
+    p = P(L, 1000)
+    bp = ctypes.byref(p)
+    f = FAKE
+    lib = L.lib()
+    A = L.grid_array
+
+    def many(*specs, count=None):
+        arr = (A * max(len(specs), 1))()
+        for d, (src, dst, rb) in zip(arr, specs):
+            d.origen, d.destino, d.record_bytes = src, dst, rb
+        return lib.grid_reorder_many(f, arr, len(specs) if count is None else count, f + (1 << 34), bp, None)
+
+    assert many((f + (1 << 30), f + (2 << 30), 32), count=0) == EINVAL          # no arrays
+    assert many(*[(f + (i << 30), f + ((i + 8) << 30), 32) for i in range(1, 6)]) == EINVAL   # five arrays
+    assert many((f + (1 << 30), f + (2 << 30), 24)) == EINVAL                   # not a multiple of 16
+    assert many((f + (1 << 30), f + (2 << 30), 512)) == EINVAL                  # above 256 bytes
+    assert many((f + (1 << 30) + 8, f + (2 << 30), 32)) == EINVAL               # misaligned origen
+    assert many((f + (1 << 30), f + (1 << 30) + 64, 32)) == EINVAL              # destino inside its origen
+    assert many((f + (1 << 30), f + (2 << 30), 32), (f + (3 << 30), f + (2 << 30), 32)) == EINVAL  # shared destino
+    assert many((f + (1 << 30), f + (2 << 30), 32), (f + (2 << 30), f + (3 << 30), 32)) == EINVAL  # destino is another origen
+    assert lib.grid_diagnostics(f, 64, None, bp, None) == EINVAL
+    assert lib.grid_diagnostics(f, 64, f, bp, None) == EINVAL                   # diag inside conteos

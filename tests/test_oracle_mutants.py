@@ -35,6 +35,10 @@ MUTANTS = {
     "scatter_direction_reorder": (
         "memcpy(dst + ORACLE_RECORD_BYTES * k, src + ORACLE_RECORD_BYTES * (uint64_t)ordenado[k],",
         "memcpy(dst + ORACLE_RECORD_BYTES * (uint64_t)ordenado[k], src + ORACLE_RECORD_BYTES * k,"),
+    "overflow_off_by_one": ("if (previo + 1u > capacidad)", "if (previo > capacidad)"),
+    "max_of_previo": ("            diag[0] = previo + 1u;", "            diag[0] = previo;"),
+    "records_scatter_direction": ("memcpy(dst + (uint64_t)record_bytes * k, src + (uint64_t)record_bytes * ordenado[k], record_bytes);",
+                                  "memcpy(dst + (uint64_t)record_bytes * ordenado[k], src + (uint64_t)record_bytes * k, record_bytes);"),
     "half_record_copied": ("               ORACLE_RECORD_BYTES);", "               ORACLE_RECORD_BYTES / 2);"),
 }
 

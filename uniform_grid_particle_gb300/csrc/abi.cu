@@ -238,6 +238,53 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
     return cuda_code(e);
 }
 
+int grid_reorder_many(const uint32_t *ordenado, const grid_array *arrays, uint32_t count, void *ws,
+                      const grid_params *p, void *stream) {
+    if (!check_params(p, nullptr) || arrays == nullptr || count == 0 || count > (uint32_t)kMaxArrays)
+        return GRID_EINVAL;
+    const uint64_t n = p->conteo;
+    if (!array_ok(ordenado, n, 4) || !array_ok(ws, kHeaderBytes, 256)) return GRID_EINVAL;
+    ManyArrays m{};
+    Span spans[2 + 2 * kMaxArrays];
+    int k = 0;
+    spans[k++] = {ordenado, n * 4};
+    spans[k++] = {ws, kHeaderBytes};
+    m.first[0] = 0;
+    for (uint32_t a = 0; a < count; ++a) {
+        const uint32_t rb = arrays[a].record_bytes;
+        if (rb == 0 || rb % 16 || rb > 256) return GRID_EINVAL;
+        if (!array_ok(arrays[a].origen, n, 16) || !array_ok(arrays[a].destino, n, 16)) return GRID_EINVAL;
+        m.src[a] = static_cast<const uint4 *>(arrays[a].origen);
+        m.dst[a] = static_cast<uint4 *>(arrays[a].destino);
+        m.pieces[a] = rb / 16;
+        m.first[a + 1] = m.first[a] + rb / 16;
+        spans[k++] = {arrays[a].destino, n * rb};
+    }
+    // Destinations must not overlap each other, ordenado, the workspace, or any origen.
+    if (!disjoint(spans, k)) return GRID_EINVAL;
+    for (uint32_t a = 0; a < count; ++a) {
+        for (uint32_t b = 0; b < count; ++b) {
+            const Span pair[] = {{arrays[a].origen, n * arrays[a].record_bytes},
+                                 {arrays[b].destino, n * arrays[b].record_bytes}};
+            if (!disjoint(pair, 2)) return GRID_EINVAL;
+        }
+    }
+    m.count = count;
+    m.per_record = m.first[count];
+    return cuda_code(launch_reorder_many(ordenado, m, p->conteo, &header(ws)->status,
+                                         static_cast<cudaStream_t>(stream), true));
+}
+
+int grid_diagnostics(const uint32_t *conteos, uint32_t capacidad, uint32_t *diag,
+                     const grid_params *p, void *stream) {
+    if (!check_params(p, nullptr)) return GRID_EINVAL;
+    const uint64_t c = p->celdas;
+    if (!array_ok(conteos, c, 16) || !array_ok(diag, 2, 4)) return GRID_EINVAL;
+    const Span s[] = {{conteos, c * 4}, {diag, 8}};
+    if (!disjoint(s, 2)) return GRID_EINVAL;
+    return cuda_code(launch_diagnostics(conteos, c, capacidad, diag, static_cast<cudaStream_t>(stream)));
+}
+
 int grid_status(void *ws, void *stream) {
     if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 256) return GRID_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -131,16 +131,6 @@ __device__ void grid_barrier(grid_ws_header *hdr, uint32_t &passed) {
     __syncthreads();
 }
 
-__device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v) {
-    const uint32_t lane = lane_id();
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= (uint32_t)o) v += t;
-    }
-    return v;
-}
-
 // Block-wide sum (every thread gets it).
 __device__ uint32_t block_sum(uint32_t v, uint32_t *s_red) {
     v = __reduce_add_sync(0xffffffffu, v);
@@ -151,24 +141,6 @@ __device__ uint32_t block_sum(uint32_t v, uint32_t *s_red) {
     for (int w = 0; w < kWarps; ++w) t += s_red[w];
     __syncthreads();
     return t;
-}
-
-// Block-wide exclusive scan; `total` receives the block's sum.
-__device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t *s_red, uint32_t &total) {
-    const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
-    const uint32_t incl = warp_inclusive_sum(v);
-    if (lane == 31) s_red[warp] = incl;
-    __syncthreads();
-    uint32_t before = 0;
-    total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const uint32_t t = s_red[w];
-        before += (uint32_t)w < warp ? t : 0u;
-        total += t;
-    }
-    __syncthreads();
-    return before + incl - v;
 }
 
 // Exclusive scans of kScanVecs rows at once: row q holds one value per
@@ -275,7 +247,6 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
     __shared__ uint32_t s_clean;
     __shared__ uint32_t s_rows[kScanVecs][kWarps];
     const uint32_t tid = threadIdx.x;
-    const uint32_t lane = tid & 31u;
     const uint32_t ctas = gridDim.x;
     uint32_t passed = 0;  // grid barriers passed (thread 0)
     // Read before this CTA's first arrival, hence before anyone changes it.

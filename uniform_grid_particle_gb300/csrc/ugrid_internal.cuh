@@ -94,6 +94,23 @@ cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *d
                                uint32_t *counts, bool stable, uint32_t *queue,
                                uint32_t queue_capacity, uint32_t *sort_scratch, cudaStream_t s);
 
+// Several arrays gathered with one ordenado (grid_reorder_many).
+constexpr int kMaxArrays = 4;
+struct ManyArrays {
+    const uint4 *src[kMaxArrays];
+    uint4 *dst[kMaxArrays];
+    uint32_t pieces[kMaxArrays];     // 16-byte pieces per record of each array
+    uint32_t first[kMaxArrays + 1];  // running sum of pieces: array a owns [first[a], first[a+1])
+    uint32_t count;                  // arrays in use
+    uint32_t per_record;             // pieces of all arrays for one record
+};
+cudaError_t launch_reorder_many(const uint32_t *ordenado, const ManyArrays &m, uint32_t n,
+                                uint32_t *status, cudaStream_t s, bool pdl);
+
+// diag[0] = max over cells of conteos, diag[1] = sum of max(0, conteos - capacidad).
+cudaError_t launch_diagnostics(const uint32_t *conteos, uint64_t cells, uint32_t capacidad,
+                               uint32_t *diag, cudaStream_t s);
+
 // Queue entries needed for cells longer than the register tier (<= cells).
 size_t segment_queue_capacity(uint64_t n, uint64_t cells);
 

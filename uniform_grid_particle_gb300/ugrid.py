@@ -45,6 +45,12 @@ class grid_params(ctypes.Structure):
     ]
 
 
+class grid_array(ctypes.Structure):
+    """Mirror of ``grid_array`` in include/ugrid.h."""
+
+    _fields_ = [("origen", ctypes.c_void_p), ("destino", ctypes.c_void_p), ("record_bytes", ctypes.c_uint32)]
+
+
 def make_params(n: int, dims, origin, cell_size: float) -> grid_params:
     p = grid_params()
     p.conteo = int(n)
@@ -83,6 +89,8 @@ def lib() -> ctypes.CDLL:
             "grid_build": ([vp, vp, vp, vp, vp, vp, vp, u, pp, vp], ctypes.c_int),
             "grid_status": ([vp, vp], ctypes.c_int),
             "grid_scan_noalloc": ([vp, vp, pp, vp], ctypes.c_int),
+            "grid_diagnostics": ([vp, ctypes.c_uint32, vp, pp, vp], ctypes.c_int),
+            "grid_reorder_many": ([vp, ctypes.POINTER(grid_array), ctypes.c_uint32, vp, pp, vp], ctypes.c_int),
             "grid_error_string": ([ctypes.c_int], ctypes.c_char_p),
         }
         for name, (args, res) in sigs.items():
@@ -192,6 +200,32 @@ def grid_scan_noalloc(conteos, inicios, p: grid_params, stream=None) -> None:
     _check(lib().grid_scan_noalloc(_u32(conteos, "conteos", p.celdas),
                                    _u32(inicios, "inicios", p.celdas + 1), ctypes.byref(p),
                                    _stream(stream)), "grid_scan_noalloc")
+
+
+def grid_reorder_many(ordenado, pairs, ws, p: grid_params, stream=None) -> None:
+    """pairs: list of (origen, destino) CUDA tensors with N rows each; every
+    row of an array is one record (its byte size a multiple of 16)."""
+    if not 1 <= len(pairs) <= 4:
+        raise ValueError("between 1 and 4 arrays")
+    descs = (grid_array * len(pairs))()
+    n = int(p.conteo)
+    for d, (src, dst) in zip(descs, pairs):
+        for t, name in ((src, "origen"), (dst, "destino")):
+            if not t.is_cuda or not t.is_contiguous() or t.shape[0] != n:
+                raise ValueError(f"{name} must be a contiguous CUDA tensor with {n} rows")
+        if src.dtype != dst.dtype or src.shape != dst.shape:
+            raise ValueError("origen and destino must have the same dtype and shape")
+        d.origen = src.data_ptr() or None
+        d.destino = dst.data_ptr() or None
+        d.record_bytes = (src.numel() * src.element_size()) // n if n else 16
+    _check(lib().grid_reorder_many(_u32(ordenado, "ordenado", n), descs, len(pairs), _ws(ws), ctypes.byref(p),
+                                   _stream(stream)), "grid_reorder_many")
+
+
+def grid_diagnostics(conteos, diag, p: grid_params, capacidad: int = 64, stream=None) -> None:
+    """diag[0] = maxPorCelda, diag[1] = desbordes for the given capacity."""
+    _check(lib().grid_diagnostics(_u32(conteos, "conteos", p.celdas), capacidad, _u32(diag, "diag", 2),
+                                  ctypes.byref(p), _stream(stream)), "grid_diagnostics")
 
 
 def grid_status(ws, stream=None) -> int:
