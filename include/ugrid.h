@@ -215,6 +215,24 @@ typedef struct grid_array {
 int grid_reorder_many(const uint32_t *ordenado, const grid_array *arrays, uint32_t count, void *ws,
                       const grid_params *p, void *stream);
 
+/* Neighbour density, the query the grid is built for ("Construir el índice…",
+ * §La dispersión: a cell is the range [inicios[c], inicios[c+1]) of the
+ * cell order; "Reordenar por celda…", §Qué cuesta la indirección and §El
+ * orden de las celdas: the neighbour loop visits the 27 cells around the
+ * particle).  For the particle at cell-order position k and radius h:
+ *   rho[k] = sum over particles j with |x_j - x_k| < h of
+ *            masa_j * (h^2 - |x_j - x_k|^2)^3        (itself included)
+ * in fp32.  Two ways to read the particles, with the same result:
+ *   ordenado == NULL  parts is the reordered destino of a build (contiguous
+ *                     reads, the point of the reorder);
+ *   ordenado != NULL  parts is the original origen, read at ordenado[j]
+ *                     (the indirection the reorder removes).
+ * inicios: u32[C+1] of the same build.  rho: float[N] (written).
+ * 0 < h <= cellSize (so the 27 cells hold every neighbour), else GRID_EINVAL.
+ * An index >= N read from ordenado sets status bit 1 and is skipped. */
+int grid_density(const ugrid_particula *parts, const uint32_t *ordenado, const uint32_t *inicios, float h,
+                 float *rho, void *ws, const grid_params *p, void *stream);
+
 /* Overflow diagnostics ("Contar partículas por celda", §Detectar el
  * desbordamiento sin salir de la GPU): for a per-cell capacity, the largest
  * occupancy (maxPorCelda: the page's atomicMax of previo + 1 while counting)

@@ -59,9 +59,11 @@ class Oracle:
         lib.oracle_canonicalise.argtypes = [_u32p, u64, _u32p]
         lib.oracle_diagnostics.argtypes = [_u32p, u64, u64, ctypes.c_uint32, _u32p, _u32p]
         lib.oracle_reorder_records.argtypes = [_u32p, u64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32]
+        lib.oracle_density.argtypes = [_f32p, u64, _u32p, _f32p, ctypes.c_float, _u32p, _u32p,
+                                       ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
         for f in ("oracle_cell_index", "oracle_histogram", "oracle_exclusive_scan",
                   "oracle_scatter", "oracle_reorder", "oracle_build", "oracle_canonicalise",
-                  "oracle_diagnostics", "oracle_reorder_records"):
+                  "oracle_diagnostics", "oracle_reorder_records", "oracle_density"):
             getattr(lib, f).restype = None
         self.lib = lib
 
@@ -147,6 +149,20 @@ class Oracle:
         self.lib.oracle_diagnostics(_ptr(celda_de, _u32p), celda_de.size, cells, capacidad,
                                     _ptr(cursor, _u32p), _ptr(diag, _u32p))
         return int(diag[0]), int(diag[1])
+
+    def density(self, parts, dims, origin, cell_size, inicios, ordenado, h: float) -> np.ndarray:
+        """rho[i] (float64) for every particle i of `parts` (original order),
+        walking the 27 cells around it through inicios / ordenado."""
+        parts = np.ascontiguousarray(parts, dtype=np.float32).reshape(-1, 8)
+        dims_a = np.asarray(dims, dtype=np.uint32)
+        origin_a = np.asarray(origin, dtype=np.float32)
+        inicios = np.ascontiguousarray(inicios, dtype=np.uint32)
+        ordenado = np.ascontiguousarray(ordenado, dtype=np.uint32)
+        out = np.empty(parts.shape[0], dtype=np.float64)
+        self.lib.oracle_density(_ptr(parts, _f32p), parts.shape[0], _ptr(dims_a, _u32p), _ptr(origin_a, _f32p),
+                                float(np.float32(cell_size)), _ptr(inicios, _u32p), _ptr(ordenado, _u32p),
+                                float(h), out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+        return out
 
     def canonicalise(self, inicios, ordenado) -> np.ndarray:
         """Copy of ordenado with every cell segment sorted ascending."""

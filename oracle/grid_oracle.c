@@ -183,3 +183,56 @@ void oracle_reorder_records(const uint32_t *ordenado, uint64_t n, const void *or
     for (uint64_t k = 0; k < n; ++k)
         memcpy(dst + (uint64_t)record_bytes * k, src + (uint64_t)record_bytes * ordenado[k], record_bytes);
 }
+
+/* Neighbour density, the consumer of the grid ("Construir el índice…",
+ * §La dispersión: a cell is walked as the range [inicios[c], inicios[c+1]) of
+ * ordenado; "Reordenar por celda…", §Qué cuesta la indirección and §El orden
+ * de las celdas: the neighbour loop visits the 27 cells around the particle).
+ * With interaction radius h (h <= cellSize, so every particle closer than h
+ * lies in one of the 27 cells, clamping included), for every particle i:
+ *     rho[i] = sum over j with |x_j - x_i| < h of masa_j * (h^2 - |x_j - x_i|^2)^3
+ * (a poly6-shaped kernel without its constant; the particle itself included),
+ * evaluated in double from the fp32 records, through the indirection
+ * origen[ordenado[k]]. */
+void oracle_density(const float *origen, uint64_t n, const uint32_t dims[3], const float origin[3],
+                    float cellSize, const uint32_t *inicios, const uint32_t *ordenado, double h,
+                    double *rho)
+{
+    const float invCell = 1.0f / cellSize;
+    const double h2 = h * h;
+    for (uint64_t i = 0; i < n; ++i) {
+        const float *pi = origen + ORACLE_FLOATS_PER_PARTICLE * i;
+        const uint32_t cx = axis_cell(pi[0], origin[0], invCell, dims[0]);
+        const uint32_t cy = axis_cell(pi[1], origin[1], invCell, dims[1]);
+        const uint32_t cz = axis_cell(pi[2], origin[2], invCell, dims[2]);
+        double sum = 0.0;
+        for (int dz = -1; dz <= 1; ++dz) {
+            const int64_t z = (int64_t)cz + dz;
+            if (z < 0 || z >= (int64_t)dims[2])
+                continue;
+            for (int dy = -1; dy <= 1; ++dy) {
+                const int64_t y = (int64_t)cy + dy;
+                if (y < 0 || y >= (int64_t)dims[1])
+                    continue;
+                for (int dx = -1; dx <= 1; ++dx) {
+                    const int64_t x = (int64_t)cx + dx;
+                    if (x < 0 || x >= (int64_t)dims[0])
+                        continue;
+                    const uint32_t c = linear_cell((uint32_t)x, (uint32_t)y, (uint32_t)z, dims[0], dims[1]);
+                    for (uint32_t k = inicios[c]; k < inicios[c + 1]; ++k) {
+                        const float *pj = origen + ORACLE_FLOATS_PER_PARTICLE * (uint64_t)ordenado[k];
+                        const double ex = (double)pj[0] - (double)pi[0];
+                        const double ey = (double)pj[1] - (double)pi[1];
+                        const double ez = (double)pj[2] - (double)pi[2];
+                        const double r2 = ex * ex + ey * ey + ez * ez;
+                        if (r2 < h2) {
+                            const double t = h2 - r2;
+                            sum += (double)pj[7] * t * t * t;
+                        }
+                    }
+                }
+            }
+        }
+        rho[i] = sum;
+    }
+}

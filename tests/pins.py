@@ -277,6 +277,59 @@ def pin_reorder_records(o, seed: int = 13) -> None:
         assert np.array_equal(o.reorder_records(perm, parts), o.reorder(perm, parts))
 
 
+# ---------------------------------------------------------------- neighbour density
+
+def _brute_density(rows, h):
+    """All pairs, float64 from the fp32 records: sum_j m_j (h^2 - r^2)^3 over r < h."""
+    pos = rows[:, :3].astype(np.float64)
+    m = rows[:, 7].astype(np.float64)
+    out = np.zeros(rows.shape[0])
+    for i in range(rows.shape[0]):
+        e = pos - pos[i]
+        r2 = e[:, 0] * e[:, 0] + e[:, 1] * e[:, 1] + e[:, 2] * e[:, 2]
+        t = np.where(r2 < h * h, h * h - r2, 0.0)
+        out[i] = float(np.sum(m * t * t * t))
+    return out
+
+
+def pin_density_brute_force(o, seed: int = 14) -> None:
+    """The 27-cell walk finds exactly the neighbours an all-pairs search finds,
+    inside the domain and beyond it (clamped particles), on non-cubic grids."""
+    rng = np.random.default_rng(seed)
+    for dims, cs, n in (((6, 4, 5), 0.5, 900), ((3, 3, 3), 1.0, 400), ((10, 1, 7), 0.25, 700)):
+        origin = (-1.0, 0.5, 2.0)
+        lo = np.array(origin) - 0.6
+        hi = np.array(origin) + np.array(dims) * cs + 0.6
+        rows = np.zeros((n, 8), np.float32)
+        rows[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+        rows[:, 7] = (0.5 + rng.random(n)).astype(np.float32)
+        ref = o.build(rows, dims, origin, cs)
+        for h in (cs, 0.7 * cs):
+            got = o.density(rows, dims, origin, cs, ref["inicios"], ref["ordenado"], h)
+            want = _brute_density(rows, h)
+            assert np.allclose(got, want, rtol=1e-12, atol=1e-300), f"dims {dims} h {h}"
+
+
+def pin_density_closed_forms(o) -> None:
+    dims, origin, cs, h = (8, 8, 8), (0.0, 0.0, 0.0), 1.0, 1.0
+    # one particle alone: its own mass times h^6
+    rows = _rows_at([(3.5, 3.5, 3.5)])
+    rows[:, 7] = 2.0
+    ref = o.build(rows, dims, origin, cs)
+    assert o.density(rows, dims, origin, cs, ref["inicios"], ref["ordenado"], h)[0] == 2.0
+    # two particles 0.5 apart across a cell face: each gets its own term plus
+    # the other's mass times (h^2 - 0.25)^3
+    rows = _rows_at([(3.75, 4.0, 4.0), (4.25, 4.0, 4.0)])
+    rows[:, 7] = [1.0, 3.0]
+    ref = o.build(rows, dims, origin, cs)
+    got = o.density(rows, dims, origin, cs, ref["inicios"], ref["ordenado"], h)
+    assert got.tolist() == [1.0 + 3.0 * 0.75 ** 3, 3.0 + 1.0 * 0.75 ** 3]
+    # exactly h apart: not a neighbour
+    rows = _rows_at([(3.5, 4.5, 4.0), (4.5, 4.5, 4.0)])
+    ref = o.build(rows, dims, origin, cs)
+    assert o.density(rows, dims, origin, cs, ref["inicios"], ref["ordenado"], h).tolist() == [1.0, 1.0]
+
+
 # ---------------------------------------------------------------- diagnostics
 
 def pin_diagnostics(o, seed: int = 12) -> None:
@@ -311,6 +364,8 @@ ALL_PINS = [
     pin_canonicalise,
     pin_diagnostics,
     pin_reorder_records,
+    pin_density_closed_forms,
+    pin_density_brute_force,
 ]
 
 

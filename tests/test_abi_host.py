@@ -177,3 +177,13 @@ def test_reorder_many_and_diagnostics_validation(L):
     assert many((f + (1 << 30), f + (2 << 30), 32), (f + (2 << 30), f + (3 << 30), 32)) == EINVAL  # destino is another origen
     assert lib.grid_diagnostics(f, 64, None, bp, None) == EINVAL
     assert lib.grid_diagnostics(f, 64, f, bp, None) == EINVAL                   # diag inside conteos
+
+
+def test_density_radius_rules(L):
+    p = P(L, 1000, cs=0.625)
+    bp = ctypes.byref(p)
+    f = FAKE
+    lib = L.lib()
+    for h in (0.0, -0.1, 0.7, math.nan, math.inf):       # must be 0 < h <= cellSize
+        assert lib.grid_density(f, None, f + (1 << 30), h, f + (2 << 30), f + (3 << 30), bp, None) == EINVAL
+    assert lib.grid_density(f, f, f + (1 << 30), 0.5, f + (2 << 30), f + (3 << 30), bp, None) == EINVAL  # ordenado inside parts

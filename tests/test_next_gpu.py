@@ -80,3 +80,63 @@ def test_reorder_many_rejects_index_out_of_range(ug):
     assert (da[5] == 0).all() and (db[5] == 0).all()
     ok = torch.arange(n, device="cuda") != 5
     assert torch.equal(da[ok], a[ordenado[ok].long()]) and torch.equal(db[ok], b[ordenado[ok].long()])
+
+
+def _density_case(ug, oracle_lib, rows, dims, origin, cs, h):
+    """GPU density through both access paths against the float64 oracle.
+
+    Tolerance: each term's fp32 error is at most a few ulps of h^2 inside
+    (h^2 - r^2)^3, i.e. ~3e-7 m h^6; over ~100 terms plus the fp32 running sum
+    (~100 * 2^-24 relative) that stays below 1e-4 * (rho + m_max h^6).  Terms
+    whose inclusion fp32 and float64 decide differently have r^2 within a few
+    ulps of h^2 and are ~1e-19 m h^6."""
+    got = gpu_build(ug, rows, dims, origin, cs)
+    n = rows.shape[0]
+    p = ug.make_params(n, dims, origin, cs)
+    ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
+    inicios = torch.from_numpy(got["inicios"].view(np.int32)).cuda()
+    ordenado = torch.from_numpy(got["ordenado"].view(np.int32)).cuda()
+    rho_sorted = torch.empty(n, dtype=torch.float32, device="cuda")
+    rho_indirect = torch.empty(n, dtype=torch.float32, device="cuda")
+    ug.grid_density(torch.from_numpy(got["destino"]).cuda(), inicios, rho_sorted, ws, p, h)
+    ug.grid_density(torch.from_numpy(rows).cuda(), inicios, rho_indirect, ws, p, h, ordenado=ordenado)
+    assert ug.grid_status(ws) == 0
+    a, b = rho_sorted.cpu().numpy(), rho_indirect.cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), "both paths add the same terms in the same order"
+    ref = oracle_lib.density(rows, dims, origin, cs, got["inicios"], got["ordenado"], h)
+    by_particle = np.empty(n, np.float64)
+    by_particle[got["ordenado"]] = a
+    scale = float(rows[:, 7].max()) * float(h) ** 6 if n else 0.0
+    err = np.abs(by_particle - ref)
+    assert np.all(err <= 1e-4 * (ref + scale)), f"max error {err.max()} (rho up to {ref.max()})"
+    return ref
+
+
+@pytest.mark.parametrize("name,h_frac", [("tiny", 1.0), ("headline", 1.0), ("headline", 0.6), ("contention", 1.0)])
+def test_density_matches_oracle(ug, oracle_lib, name, h_frac):
+    s = scenes.SCENES[name]
+    _density_case(ug, oracle_lib, s.particles(), s.dims, s.origin, s.cell_size, s.cell_size * h_frac)
+
+
+def test_density_sph_like(ug, oracle_lib):
+    """~25 particles per cell and ~100 neighbours within h, on a non-cubic grid
+    with particles outside the domain (clamped into the boundary cells)."""
+    rng = np.random.default_rng(21)
+    n, dims, cs = 200_000, (24, 20, 17), np.float32(0.5)
+    origin = (np.float32(-6.0), np.float32(-5.0), np.float32(-4.25))
+    lo = np.array(origin, np.float64) - 0.3
+    hi = np.array(origin, np.float64) + np.array(dims) * float(cs) + 0.3
+    rows = np.zeros((n, 8), np.float32)
+    rows[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+    rows[:, 3] = 1.0
+    rows[:, 7] = (0.5 + rng.random(n)).astype(np.float32)
+    ref = _density_case(ug, oracle_lib, rows, dims, origin, cs, cs)
+    assert float(np.median(ref)) > 0.0
+
+
+def test_density_empty_scene(ug):
+    p = ug.make_params(0, (4, 4, 4), (0, 0, 0), 1.0)
+    ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
+    inicios = torch.zeros(65, dtype=torch.int32, device="cuda")
+    ug.grid_density(None, inicios, torch.empty(0, device="cuda"), ws, p, 1.0)
+    assert ug.grid_status(ws) == 0

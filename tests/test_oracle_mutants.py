@@ -39,6 +39,9 @@ MUTANTS = {
     "max_of_previo": ("            diag[0] = previo + 1u;", "            diag[0] = previo;"),
     "records_scatter_direction": ("memcpy(dst + (uint64_t)record_bytes * k, src + (uint64_t)record_bytes * ordenado[k], record_bytes);",
                                   "memcpy(dst + (uint64_t)record_bytes * ordenado[k], src + (uint64_t)record_bytes * k, record_bytes);"),
+    "stencil_one_sided": ("for (int dz = -1; dz <= 1; ++dz) {", "for (int dz = -1; dz <= 0; ++dz) {"),
+    "radius_not_squared": ("if (r2 < h2) {", "if (r2 < h) {"),
+    "own_mass": ("sum += (double)pj[7] * t * t * t;", "sum += (double)pi[7] * t * t * t;"),
     "half_record_copied": ("               ORACLE_RECORD_BYTES);", "               ORACLE_RECORD_BYTES / 2);"),
 }
 

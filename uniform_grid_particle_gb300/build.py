@@ -19,7 +19,8 @@ OBJDIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libugrid.so")
 
 SOURCES = ["abi.cu", "build_fused.cu", "count.cu", "scan.cu", "scatter.cu", "reorder.cu", "segsort.cu",
-           "scan_noalloc.cu", "diagnostics.cu", "reorder_many.cu"]
+           "scan_noalloc.cu", "diagnostics.cu", "reorder_many.cu",
+           "density.cu"]
 HEADERS = [os.path.join(CSRC, "ugrid_internal.cuh"), os.path.join(CSRC, "segsort_device.cuh"),
            os.path.join(INCLUDE, "ugrid.h")]
 

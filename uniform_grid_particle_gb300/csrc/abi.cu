@@ -275,6 +275,22 @@ int grid_reorder_many(const uint32_t *ordenado, const grid_array *arrays, uint32
                                          static_cast<cudaStream_t>(stream), true));
 }
 
+int grid_density(const ugrid_particula *parts, const uint32_t *ordenado, const uint32_t *inicios, float h,
+                 float *rho, void *ws, const grid_params *p, void *stream) {
+    Geometry g;
+    if (!check_params(p, &g)) return GRID_EINVAL;
+    if (!std::isfinite(h) || !(h > 0.0f) || h > p->cellSize) return GRID_EINVAL;
+    const uint64_t n = p->conteo, c = p->celdas;
+    if (!array_ok(parts, n, 16) || !array_ok(inicios, c + 1, 4) || !array_ok(rho, n, 4) ||
+        !array_ok(ws, kHeaderBytes, 256) || (ordenado != nullptr && !array_ok(ordenado, n, 4)))
+        return GRID_EINVAL;
+    const Span s[] = {{rho, n * 4}, {parts, n * kRecord}, {inicios, (c + 1) * 4},
+                      {ordenado, ordenado ? n * 4 : 0}, {ws, kHeaderBytes}};
+    if (!disjoint(s, 5)) return GRID_EINVAL;
+    return cuda_code(launch_density(parts, ordenado, inicios, g, h, p->conteo, rho, &header(ws)->status,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
 int grid_diagnostics(const uint32_t *conteos, uint32_t capacidad, uint32_t *diag,
                      const grid_params *p, void *stream) {
     if (!check_params(p, nullptr)) return GRID_EINVAL;

@@ -107,6 +107,12 @@ struct ManyArrays {
 cudaError_t launch_reorder_many(const uint32_t *ordenado, const ManyArrays &m, uint32_t n,
                                 uint32_t *status, cudaStream_t s, bool pdl);
 
+// rho[k] = neighbour density of the particle at cell-order position k (parts =
+// destino when ordenado is null, else origen read through ordenado).
+cudaError_t launch_density(const ugrid_particula *parts, const uint32_t *ordenado,
+                           const uint32_t *inicios, const Geometry &g, float h, uint32_t n,
+                           float *rho, uint32_t *status, cudaStream_t s);
+
 // diag[0] = max over cells of conteos, diag[1] = sum of max(0, conteos - capacidad).
 cudaError_t launch_diagnostics(const uint32_t *conteos, uint64_t cells, uint32_t capacidad,
                                uint32_t *diag, cudaStream_t s);

@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
             "grid_status": ([vp, vp], ctypes.c_int),
             "grid_scan_noalloc": ([vp, vp, pp, vp], ctypes.c_int),
             "grid_diagnostics": ([vp, ctypes.c_uint32, vp, pp, vp], ctypes.c_int),
+            "grid_density": ([vp, vp, vp, ctypes.c_float, vp, vp, pp, vp], ctypes.c_int),
             "grid_reorder_many": ([vp, ctypes.POINTER(grid_array), ctypes.c_uint32, vp, pp, vp], ctypes.c_int),
             "grid_error_string": ([ctypes.c_int], ctypes.c_char_p),
         }
@@ -220,6 +221,16 @@ def grid_reorder_many(ordenado, pairs, ws, p: grid_params, stream=None) -> None:
         d.record_bytes = (src.numel() * src.element_size()) // n if n else 16
     _check(lib().grid_reorder_many(_u32(ordenado, "ordenado", n), descs, len(pairs), _ws(ws), ctypes.byref(p),
                                    _stream(stream)), "grid_reorder_many")
+
+
+def grid_density(parts, inicios, rho, ws, p: grid_params, h: float, ordenado=None, stream=None) -> None:
+    """rho[k] for the particle at cell-order position k: parts is destino when
+    ordenado is None, else origen read through ordenado."""
+    _check(lib().grid_density(_parts(parts, "parts", p.conteo),
+                              None if ordenado is None else _u32(ordenado, "ordenado", p.conteo),
+                              _u32(inicios, "inicios", p.celdas + 1), float(np.float32(h)),
+                              _ptr(rho, "rho", p.conteo, (torch.float32,)), _ws(ws), ctypes.byref(p),
+                              _stream(stream)), "grid_density")
 
 
 def grid_diagnostics(conteos, diag, p: grid_params, capacidad: int = 64, stream=None) -> None:
