@@ -49,18 +49,21 @@ class Oracle:
         self.path = path
         lib = ctypes.CDLL(path)
         u64 = ctypes.c_uint64
-        lib.oracle_cell_index.argtypes = [_f32p, u64, _u32p, _f32p, ctypes.c_float, _u32p]
+        u32 = ctypes.c_uint32
+        lib.oracle_cell_index.argtypes = [_f32p, u64, _u32p, _f32p, ctypes.c_float, u32, _u32p]
         lib.oracle_histogram.argtypes = [_u32p, u64, _u32p, u64]
         lib.oracle_exclusive_scan.argtypes = [_u32p, u64, _u32p]
         lib.oracle_scatter.argtypes = [_u32p, u64, _u32p, _u32p, u64, _u32p]
         lib.oracle_reorder.argtypes = [_u32p, u64, ctypes.c_void_p, ctypes.c_void_p]
-        lib.oracle_build.argtypes = [_f32p, u64, _u32p, _f32p, ctypes.c_float,
+        lib.oracle_build.argtypes = [_f32p, u64, _u32p, _f32p, ctypes.c_float, u32,
                                      _u32p, _u32p, _u32p, _u32p, _f32p]
         lib.oracle_canonicalise.argtypes = [_u32p, u64, _u32p]
         lib.oracle_diagnostics.argtypes = [_u32p, u64, u64, ctypes.c_uint32, _u32p, _u32p]
         lib.oracle_reorder_records.argtypes = [_u32p, u64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32]
-        lib.oracle_density.argtypes = [_f32p, u64, _u32p, _f32p, ctypes.c_float, _u32p, _u32p,
+        lib.oracle_density.argtypes = [_f32p, u64, _u32p, _f32p, ctypes.c_float, u32, _u32p, _u32p,
                                        ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
+        lib.oracle_morton_cell.argtypes = [u32, u32, u32, _u32p]
+        lib.oracle_morton_cell.restype = u32
         for f in ("oracle_cell_index", "oracle_histogram", "oracle_exclusive_scan",
                   "oracle_scatter", "oracle_reorder", "oracle_build", "oracle_canonicalise",
                   "oracle_diagnostics", "oracle_reorder_records", "oracle_density"):
@@ -68,13 +71,13 @@ class Oracle:
         self.lib = lib
 
     # -- one function per step ------------------------------------------------
-    def cell_index(self, parts, dims, origin, cell_size) -> np.ndarray:
+    def cell_index(self, parts, dims, origin, cell_size, order: int = 0) -> np.ndarray:
         parts = np.ascontiguousarray(parts, dtype=np.float32).reshape(-1, 8)
         dims_a = np.asarray(dims, dtype=np.uint32)
         origin_a = np.asarray(origin, dtype=np.float32)
         out = np.empty(parts.shape[0], dtype=np.uint32)
         self.lib.oracle_cell_index(_ptr(parts, _f32p), parts.shape[0], _ptr(dims_a, _u32p),
-                                   _ptr(origin_a, _f32p), float(np.float32(cell_size)),
+                                   _ptr(origin_a, _f32p), float(np.float32(cell_size)), order,
                                    _ptr(out, _u32p))
         return out
 
@@ -121,7 +124,7 @@ class Oracle:
                                         out.ctypes.data_as(ctypes.c_void_p), rb)
         return out
 
-    def build(self, parts, dims, origin, cell_size) -> dict:
+    def build(self, parts, dims, origin, cell_size, order: int = 0) -> dict:
         """The whole chain; returns conteos, celdaDe, inicios, ordenado, destino."""
         parts = np.ascontiguousarray(parts, dtype=np.float32).reshape(-1, 8)
         n = parts.shape[0]
@@ -136,7 +139,7 @@ class Oracle:
             "destino": np.empty((n, 8), dtype=np.float32),
         }
         self.lib.oracle_build(_ptr(parts, _f32p), n, _ptr(dims_a, _u32p), _ptr(origin_a, _f32p),
-                              float(np.float32(cell_size)), _ptr(out["conteos"], _u32p),
+                              float(np.float32(cell_size)), order, _ptr(out["conteos"], _u32p),
                               _ptr(out["celdaDe"], _u32p), _ptr(out["inicios"], _u32p),
                               _ptr(out["ordenado"], _u32p), _ptr(out["destino"], _f32p))
         return out
@@ -150,7 +153,7 @@ class Oracle:
                                     _ptr(cursor, _u32p), _ptr(diag, _u32p))
         return int(diag[0]), int(diag[1])
 
-    def density(self, parts, dims, origin, cell_size, inicios, ordenado, h: float) -> np.ndarray:
+    def density(self, parts, dims, origin, cell_size, inicios, ordenado, h: float, order: int = 0) -> np.ndarray:
         """rho[i] (float64) for every particle i of `parts` (original order),
         walking the 27 cells around it through inicios / ordenado."""
         parts = np.ascontiguousarray(parts, dtype=np.float32).reshape(-1, 8)
@@ -160,9 +163,13 @@ class Oracle:
         ordenado = np.ascontiguousarray(ordenado, dtype=np.uint32)
         out = np.empty(parts.shape[0], dtype=np.float64)
         self.lib.oracle_density(_ptr(parts, _f32p), parts.shape[0], _ptr(dims_a, _u32p), _ptr(origin_a, _f32p),
-                                float(np.float32(cell_size)), _ptr(inicios, _u32p), _ptr(ordenado, _u32p),
+                                float(np.float32(cell_size)), order, _ptr(inicios, _u32p), _ptr(ordenado, _u32p),
                                 float(h), out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
         return out
+
+    def morton_cell(self, x: int, y: int, z: int, dims) -> int:
+        dims_a = np.asarray(dims, dtype=np.uint32)
+        return int(self.lib.oracle_morton_cell(x, y, z, _ptr(dims_a, _u32p)))
 
     def canonicalise(self, inicios, ordenado) -> np.ndarray:
         """Copy of ordenado with every cell segment sorted ascending."""

@@ -61,9 +61,51 @@ static uint32_t linear_cell(uint32_t x, uint32_t y, uint32_t z, uint32_t gx, uin
     return x + y * gx + z * gx * gy;
 }
 
-/* [count] celdaDe[i] for every particle (parts: N rows of 8 floats). */
+/* [reorder] §El orden de las celdas, the Morton (Z-curve) alternative: the
+ * cell index interleaves the bits of x, y and z.  With dims = 2^bx, 2^by, 2^bz,
+ * level l (from the least significant) contributes bit l of x, then of y, then
+ * of z, each axis only while it still has bits; the result covers
+ * [0, 2^(bx+by+bz)) exactly once. */
+static uint32_t morton_cell(uint32_t x, uint32_t y, uint32_t z, const uint32_t bits[3])
+{
+    uint32_t code = 0u, pos = 0u;
+    for (uint32_t l = 0; l < 32u; ++l) {
+        if (l < bits[0]) code |= ((x >> l) & 1u) << pos++;
+        if (l < bits[1]) code |= ((y >> l) & 1u) << pos++;
+        if (l < bits[2]) code |= ((z >> l) & 1u) << pos++;
+    }
+    return code;
+}
+
+static uint32_t log2_exact(uint32_t d)
+{
+    uint32_t b = 0u;
+    while ((1u << b) < d)
+        ++b;
+    return b;
+}
+
+/* Cell index of one particle's clamped coordinates in the chosen order
+ * (0: linear, 1: Morton). */
+static uint32_t cell_in_order(uint32_t x, uint32_t y, uint32_t z, const uint32_t dims[3], uint32_t order)
+{
+    if (order == 1u) {
+        const uint32_t bits[3] = {log2_exact(dims[0]), log2_exact(dims[1]), log2_exact(dims[2])};
+        return morton_cell(x, y, z, bits);
+    }
+    return linear_cell(x, y, z, dims[0], dims[1]);
+}
+
+/* Morton cell index of cell (x, y, z), exported for the pins. */
+uint32_t oracle_morton_cell(uint32_t x, uint32_t y, uint32_t z, const uint32_t dims[3])
+{
+    return cell_in_order(x, y, z, dims, 1u);
+}
+
+/* [count] celdaDe[i] for every particle (parts: N rows of 8 floats), cells
+ * numbered in `order` (0: linear, 1: Morton). */
 void oracle_cell_index(const float *parts, uint64_t n, const uint32_t dims[3],
-                       const float origin[3], float cellSize, uint32_t *celdaDe)
+                       const float origin[3], float cellSize, uint32_t order, uint32_t *celdaDe)
 {
     const float invCell = 1.0f / cellSize;
     for (uint64_t i = 0; i < n; ++i) {
@@ -71,7 +113,7 @@ void oracle_cell_index(const float *parts, uint64_t n, const uint32_t dims[3],
         uint32_t x = axis_cell(pos[0], origin[0], invCell, dims[0]);
         uint32_t y = axis_cell(pos[1], origin[1], invCell, dims[1]);
         uint32_t z = axis_cell(pos[2], origin[2], invCell, dims[2]);
-        celdaDe[i] = linear_cell(x, y, z, dims[0], dims[1]);
+        celdaDe[i] = cell_in_order(x, y, z, dims, order);
     }
 }
 
@@ -118,11 +160,11 @@ void oracle_reorder(const uint32_t *ordenado, uint64_t n, const void *origen, vo
  * After it conteos holds the histogram again, as it does when the cursor
  * reuses the counter array and ends at the counts. */
 void oracle_build(const float *origen, uint64_t n, const uint32_t dims[3], const float origin[3],
-                  float cellSize, uint32_t *conteos, uint32_t *celdaDe, uint32_t *inicios,
-                  uint32_t *ordenado, float *destino)
+                  float cellSize, uint32_t order, uint32_t *conteos, uint32_t *celdaDe,
+                  uint32_t *inicios, uint32_t *ordenado, float *destino)
 {
     const uint64_t cells = (uint64_t)dims[0] * dims[1] * dims[2];
-    oracle_cell_index(origen, n, dims, origin, cellSize, celdaDe);
+    oracle_cell_index(origen, n, dims, origin, cellSize, order, celdaDe);
     oracle_histogram(celdaDe, n, conteos, cells);
     oracle_exclusive_scan(conteos, cells, inicios);
     oracle_scatter(celdaDe, n, inicios, conteos, cells, ordenado);
@@ -193,10 +235,10 @@ void oracle_reorder_records(const uint32_t *ordenado, uint64_t n, const void *or
  *     rho[i] = sum over j with |x_j - x_i| < h of masa_j * (h^2 - |x_j - x_i|^2)^3
  * (a poly6-shaped kernel without its constant; the particle itself included),
  * evaluated in double from the fp32 records, through the indirection
- * origen[ordenado[k]]. */
+ * origen[ordenado[k]], with the cells numbered in `order`. */
 void oracle_density(const float *origen, uint64_t n, const uint32_t dims[3], const float origin[3],
-                    float cellSize, const uint32_t *inicios, const uint32_t *ordenado, double h,
-                    double *rho)
+                    float cellSize, uint32_t order, const uint32_t *inicios, const uint32_t *ordenado,
+                    double h, double *rho)
 {
     const float invCell = 1.0f / cellSize;
     const double h2 = h * h;
@@ -218,7 +260,7 @@ void oracle_density(const float *origen, uint64_t n, const uint32_t dims[3], con
                     const int64_t x = (int64_t)cx + dx;
                     if (x < 0 || x >= (int64_t)dims[0])
                         continue;
-                    const uint32_t c = linear_cell((uint32_t)x, (uint32_t)y, (uint32_t)z, dims[0], dims[1]);
+                    const uint32_t c = cell_in_order((uint32_t)x, (uint32_t)y, (uint32_t)z, dims, order);
                     for (uint32_t k = inicios[c]; k < inicios[c + 1]; ++k) {
                         const float *pj = origen + ORACLE_FLOATS_PER_PARTICLE * (uint64_t)ordenado[k];
                         const double ex = (double)pj[0] - (double)pi[0];

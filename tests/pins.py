@@ -13,7 +13,10 @@ truth are:
 * independent library routines for whole steps: ``numpy.bincount`` (histogram),
   ``numpy.cumsum`` (scan), a stable ``numpy.argsort`` (scatter), numpy fancy
   indexing (gather);
-* a pure-Python brute force on tiny inputs.
+* a pure-Python brute force on tiny inputs;
+* for the Morton order, a hand-interleaved table (``golden/morton_cell_index.txt``),
+  bijection and aligned-block contiguity, and the XOR comparison of two cells
+  (a definition of the Z-curve order that builds no code).
 """
 from __future__ import annotations
 
@@ -350,6 +353,109 @@ def pin_diagnostics(o, seed: int = 12) -> None:
         assert o.diagnostics(celda, cells, cap) == want
 
 
+# ---------------------------------------------------------------- Morton order
+
+def _centres(dims, origin, cs, cells_xyz):
+    return _rows_at([(origin[0] + (x + 0.5) * cs, origin[1] + (y + 0.5) * cs, origin[2] + (z + 0.5) * cs)
+                     for x, y, z in cells_xyz])
+
+
+def _all_cells(dims):
+    gx, gy, gz = dims
+    return [(x, y, z) for z in range(gz) for y in range(gy) for x in range(gx)]
+
+
+def pin_morton_index_table(o) -> None:
+    """Hand-interleaved Morton codes on cubic and unequal power-of-two grids,
+    through the exported helper and through the cell index of cell centres."""
+    origin, cs = (-1.0, 2.0, 0.5), 0.25
+    for row in read_golden("morton_cell_index.txt"):
+        gx, gy, gz, x, y, z, idx = (int(v) for v in row)
+        assert o.morton_cell(x, y, z, (gx, gy, gz)) == idx, f"{row}"
+        got = o.cell_index(_centres((gx, gy, gz), origin, cs, [(x, y, z)]), (gx, gy, gz), origin, cs, order=1)
+        assert int(got[0]) == idx, f"cell index of {row}: {int(got[0])}"
+
+
+def pin_morton_bijection_and_blocks(o) -> None:
+    """The Morton index is a bijection onto [0, cells), and every aligned
+    2^k x 2^k x 2^k block of a cubic grid (2x2x2 blocks on every grid whose
+    sides are all >= 2) holds one contiguous range of codes starting at a
+    multiple of its size: the locality the page wants from the Z-curve."""
+    origin, cs = (0.0, 0.0, 0.0), 1.0
+    for dims in ((4, 4, 4), (8, 2, 4), (16, 8, 2), (1, 8, 4), (2, 1, 1), (16, 16, 16), (32, 4, 8)):
+        cells = _all_cells(dims)
+        codes = o.cell_index(_centres(dims, origin, cs, cells), dims, origin, cs, order=1).astype(np.int64)
+        assert np.array_equal(np.sort(codes), np.arange(len(cells))), f"not a bijection on {dims}"
+        xyz = np.array(cells, dtype=np.int64)
+        sides = [1]
+        if min(dims) >= 2:
+            sides.append(2)
+        if dims[0] == dims[1] == dims[2]:
+            sides = [1 << k for k in range(int(math.log2(dims[0])) + 1)]
+        for side in sides:
+            key = (xyz[:, 0] // side) + dims[0] * ((xyz[:, 1] // side) + dims[1] * (xyz[:, 2] // side))
+            for b in np.unique(key):
+                block = np.sort(codes[key == b])
+                size = side ** 3
+                assert block.size == size and block[0] % size == 0 and block[-1] - block[0] == size - 1, (
+                    f"{side}-block {b} of {dims} is not contiguous: {block[:4]}..")
+
+
+def _zorder_less(a, b) -> int:
+    """Comparison of two cells by the most significant differing bit of any
+    coordinate (Chan's XOR test): the axis whose XOR has the highest bit
+    decides, z outranking y outranking x at equal bit position.  This is the
+    order of the Z-curve on a cubic grid, stated without building a code."""
+    rank = max(((a[k] ^ b[k]).bit_length(), k) for k in (0, 1, 2))
+    if rank[0] == 0:
+        return 0
+    k = rank[1]
+    return -1 if a[k] < b[k] else 1
+
+
+def pin_morton_matches_xor_comparator(o) -> None:
+    """On cubic grids the Morton order of the cells is the order given by the
+    XOR comparison, a definition that never interleaves bits."""
+    import functools
+    origin, cs = (0.0, 0.0, 0.0), 1.0
+    for dims in ((8, 8, 8), (16, 16, 16)):
+        cells = _all_cells(dims)
+        codes = o.cell_index(_centres(dims, origin, cs, cells), dims, origin, cs, order=1)
+        by_code = [cells[i] for i in np.argsort(codes, kind="stable")]
+        by_xor = sorted(cells, key=functools.cmp_to_key(_zorder_less))
+        assert by_code == by_xor, f"Morton order differs from the XOR comparison on {dims}"
+
+
+def pin_build_orders_agree(o, seed: int = 15) -> None:
+    """A build in Morton order is the linear build with its cells relabelled:
+    the same particles fall in the same physical cell, every cell keeps its
+    count and its members, and the neighbour density does not depend on the
+    order (same neighbour sets; sums compared to rounding)."""
+    rng = np.random.default_rng(seed)
+    for dims, cs, n in (((8, 4, 16), 0.5, 3000), ((4, 4, 4), 1.0, 600), ((2, 8, 1), 0.75, 300)):
+        origin = (-0.3, 1.0, 0.2)
+        lo = np.array(origin) - 0.4
+        hi = np.array(origin) + np.array(dims) * cs + 0.4
+        rows = np.zeros((n, 8), np.float32)
+        rows[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+        rows[:, 7] = (0.5 + rng.random(n)).astype(np.float32)
+        lin = o.build(rows, dims, origin, cs, order=0)
+        mor = o.build(rows, dims, origin, cs, order=1)
+        cells = _all_cells(dims)
+        relabel = o.cell_index(_centres(dims, origin, cs, cells), dims, origin, cs, order=1)
+        assert np.array_equal(relabel[lin["celdaDe"]], mor["celdaDe"]), f"celdaDe differs on {dims}"
+        assert np.array_equal(mor["conteos"][relabel], lin["conteos"]), f"conteos differ on {dims}"
+        for c_lin, c_mor in enumerate(relabel):
+            a = lin["ordenado"][lin["inicios"][c_lin]:lin["inicios"][c_lin + 1]]
+            b = mor["ordenado"][mor["inicios"][c_mor]:mor["inicios"][c_mor + 1]]
+            assert np.array_equal(a, b), f"members of cell {c_lin} differ on {dims}"
+        for h in (cs, 0.6 * cs):
+            d_lin = o.density(rows, dims, origin, cs, lin["inicios"], lin["ordenado"], h, order=0)
+            d_mor = o.density(rows, dims, origin, cs, mor["inicios"], mor["ordenado"], h, order=1)
+            assert np.allclose(d_mor, d_lin, rtol=1e-12, atol=0.0), f"density depends on the order ({dims}, h={h})"
+            assert np.allclose(d_mor, _brute_density(rows, h), rtol=1e-12, atol=1e-300)
+
+
 ALL_PINS = [
     pin_cell_index_special_positions,
     pin_linear_index_table,
@@ -366,6 +472,10 @@ ALL_PINS = [
     pin_reorder_records,
     pin_density_closed_forms,
     pin_density_brute_force,
+    pin_morton_index_table,
+    pin_morton_bijection_and_blocks,
+    pin_morton_matches_xor_comparator,
+    pin_build_orders_agree,
 ]
 
 

@@ -43,6 +43,17 @@ MUTANTS = {
     "radius_not_squared": ("if (r2 < h2) {", "if (r2 < h) {"),
     "own_mass": ("sum += (double)pj[7] * t * t * t;", "sum += (double)pi[7] * t * t * t;"),
     "half_record_copied": ("               ORACLE_RECORD_BYTES);", "               ORACLE_RECORD_BYTES / 2);"),
+    "morton_x_bit_from_y": ("if (l < bits[0]) code |= ((x >> l) & 1u) << pos++;",
+                            "if (l < bits[0]) code |= ((y >> l) & 1u) << pos++;"),
+    "morton_position_not_advanced": ("if (l < bits[2]) code |= ((z >> l) & 1u) << pos++;",
+                                     "if (l < bits[2]) code |= ((z >> l) & 1u) << pos;"),
+    "morton_y_before_x": ("if (l < bits[1]) code |= ((y >> l) & 1u) << pos++;",
+                          "if (l < bits[1]) code |= ((y >> l) & 1u) << (pos++ - 1u);"),
+    "morton_bits_rounded_up": ("while ((1u << b) < d)", "while ((1u << b) <= d)"),
+    "morton_shared_bit_count": ("log2_exact(dims[1]), log2_exact(dims[2])", "log2_exact(dims[0]), log2_exact(dims[2])"),
+    "order_ignored_by_count": ("celdaDe[i] = cell_in_order(x, y, z, dims, order);",
+                               "celdaDe[i] = cell_in_order(x, y, z, dims, 0u);"),
+    "order_ignored_by_density": ("(uint32_t)z, dims, order);", "(uint32_t)z, dims, 0u);"),
 }
 
 RUNNER = """
