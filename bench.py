@@ -13,6 +13,10 @@ Further passes in the same run:
                    per-kernel microseconds and the gather kernel's roofline;
   * end to end   — host buffers: pinned host origen -> device, build,
                    destino and inicios -> pinned host, all inside the events;
+  * neighbours   — the neighbour query on an SPH-like scene (5.2M particles,
+                   64^3 cells, ~84 neighbours), in linear and Morton cell
+                   order, on the reordered records and through ordenado:
+                   the reorder's gain and the Z-curve's;
   * cpu baseline — the CPU oracle (single thread) on the same scene.
 
 ``--impl reference`` times the CPU oracle alone (the reference arm).
@@ -397,6 +401,47 @@ def run_gpu(args) -> None:
     if not np.array_equal(host_inicios.numpy()[[0, cells]], np.array([0, n], dtype=np.int32)):
         raise RuntimeError("end-to-end result is inconsistent")
 
+    # ---- neighbour query on an SPH-like scene: cell order x access path ----
+    neighbour = None
+    if args.density_steps > 0:
+        sph = scenes.SCENES["sph"]
+        origen_s = torch.from_numpy(sph.particles()).cuda()
+        rho = torch.empty(sph.n, dtype=torch.float32, device="cuda")
+        h = sph.cell_size
+        neighbour = {
+            "scene": f"sph: N={sph.n:,}, grid {sph.dims[0]}^3, h = cellSize = {h:.6f}",
+            "mean_particles_per_cell": sph.n / sph.cells,
+            "l2": "flushed between steps",
+        }
+        for order_name, order in (("linear", ug.GRID_ORDER_LINEAR), ("morton", ug.GRID_ORDER_MORTON)):
+            ps = ug.make_params(sph.n, sph.dims, sph.origin, sph.cell_size, order=order)
+            bs = ug.GridBuffers.allocate(ps)
+            bs.build(origen_s, ps, stream=stream)
+
+            def q_sorted():
+                ug.grid_density(bs.destino, bs.inicios, rho, bs.ws, ps, h, stream=stream)
+
+            def q_indirect():
+                ug.grid_density(origen_s, bs.inicios, rho, bs.ws, ps, h, ordenado=bs.ordenado, stream=stream)
+
+            for k in range(args.warmup):
+                settle(k)
+                q_sorted()
+                q_indirect()
+            sorted_ms = statistics.mean(timed(q_sorted, args.density_steps))
+            indirect_ms = statistics.mean(timed(q_indirect, args.density_steps))
+            if ug.grid_status(bs.ws) != 0:
+                raise RuntimeError(f"device status {ug.grid_status(bs.ws)} after the neighbour query")
+            neighbour[f"us_{order_name}_sorted"] = 1e3 * sorted_ms
+            neighbour[f"us_{order_name}_indirect"] = 1e3 * indirect_ms
+            del bs
+        neighbour["reorder_gain"] = neighbour["us_linear_indirect"] / neighbour["us_linear_sorted"]
+        neighbour["morton_gain_sorted"] = neighbour["us_linear_sorted"] / neighbour["us_morton_sorted"]
+        neighbour["morton_gain_indirect"] = neighbour["us_linear_indirect"] / neighbour["us_morton_indirect"]
+        best = min(neighbour[f"us_{o}_sorted"] for o in ("linear", "morton"))
+        neighbour["mparticles_per_s_best"] = sph.n / best
+        del origen_s, rho
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -430,6 +475,7 @@ def run_gpu(args) -> None:
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(host_in.numel() * 4),
                 "d2h_bytes_per_step": int(host_dest.numel() * 4 + host_inicios.numel() * 4),
                 "ms_per_step": e2e_total / len(e2e_ms)},
+        "neighbour_query": neighbour,
         "gpu_launches": kernels_per_step * args.steps,
         "clocks": clocks.summary(),
     }
@@ -447,6 +493,8 @@ def main(argv=None) -> None:
     ap.add_argument("--scene", default="headline")
     ap.add_argument("--stable", action="store_true", help="time the stable (reproducible) build")
     ap.add_argument("--graph-steps", type=int, default=2000)
+    ap.add_argument("--density-steps", type=int, default=20,
+                    help="steps of the neighbour-query leg (0 skips it)")
     ap.add_argument("--phase-steps", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time")

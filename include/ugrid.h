@@ -58,16 +58,29 @@ typedef struct ugrid_particula {
  * Cell of a particle, per axis d (fp32, each operation rounded to nearest, no
  * fused multiply-add; invCell = 1.0f/cellSize rounded once on the host):
  *   q_d = clamp(floor((pos_d - origin_d) * invCell), 0, dims_d - 1)
- * with NaN mapped to 0 and +inf to dims_d - 1; the linear index is
- *   c = qx + qy*GX + qz*GX*GY
- * ("Reordenar por celda…", §El orden de las celdas). */
+ * with NaN mapped to 0 and +inf to dims_d - 1.  The cell index c follows
+ * `order` ("Reordenar por celda…", §El orden de las celdas):
+ *   GRID_ORDER_LINEAR  c = qx + qy*GX + qz*GX*GY (x fastest);
+ *   GRID_ORDER_MORTON  the Z-curve: every side a power of two (2^bx, 2^by,
+ *                      2^bz); from the least significant level l up, level l
+ *                      appends bit l of qx, then of qy, then of qz, each axis
+ *                      only while l is below its bit count.  The 27 cells
+ *                      around a cell then span a compact range of c.
+ * Every entry point that reads positions or walks cells takes the order from
+ * here; a grid must be built and walked with the same order. */
 typedef struct grid_params {
     uint32_t conteo;
     uint32_t celdas;
     uint32_t dims[3];
     float origin[3];
     float cellSize;
+    uint32_t order; /* enum grid_order */
 } grid_params;
+
+enum grid_order {
+    GRID_ORDER_LINEAR = 0u,
+    GRID_ORDER_MORTON = 1u
+};
 
 enum grid_status_code {
     GRID_OK = 0,

@@ -79,7 +79,10 @@ def _call(L, name, *args):
     lambda p: setattr(p, "cellSize", 1e-45),          # 1/cellSize overflows to inf
     lambda p: p.origin.__setitem__(1, math.nan),
     lambda p: p.origin.__setitem__(2, -math.inf),
-], ids=["celdas", "dims0", "cs0", "cs_neg", "cs_nan", "cs_inf", "cs_denorm", "origin_nan", "origin_inf"])
+    lambda p: setattr(p, "order", 2),
+    lambda p: (setattr(p, "order", 1), p.dims.__setitem__(1, 3), setattr(p, "celdas", p.dims[0] * 3 * p.dims[2])),
+], ids=["celdas", "dims0", "cs0", "cs_neg", "cs_nan", "cs_inf", "cs_denorm", "origin_nan", "origin_inf",
+        "order_unknown", "morton_not_pow2"])
 def test_bad_params_rejected_everywhere(L, mutate):
     p = P(L)
     mutate(p)
@@ -187,3 +190,12 @@ def test_density_radius_rules(L):
     for h in (0.0, -0.1, 0.7, math.nan, math.inf):       # must be 0 < h <= cellSize
         assert lib.grid_density(f, None, f + (1 << 30), h, f + (2 << 30), f + (3 << 30), bp, None) == EINVAL
     assert lib.grid_density(f, f, f + (1 << 30), 0.5, f + (2 << 30), f + (3 << 30), bp, None) == EINVAL  # ordenado inside parts
+
+
+def test_morton_accepts_power_of_two_sides(L):
+    """Morton order takes any power-of-two sides, unequal and of size 1 included."""
+    for dims in ((4, 4, 4), (8, 2, 16), (1, 1, 1), (1024, 1024, 1024), (2, 1, 1 << 20)):
+        p = L.make_params(10, dims, (0.0, 0.0, 0.0), 1.0, order=L.GRID_ORDER_MORTON)
+        assert L.grid_workspace_bytes(p, 0) > 0, dims
+    p = L.make_params(10, (4, 4, 6), (0.0, 0.0, 0.0), 1.0, order=L.GRID_ORDER_MORTON)
+    assert L.grid_workspace_bytes(p, 0) == 0

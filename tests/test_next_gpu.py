@@ -82,7 +82,7 @@ def test_reorder_many_rejects_index_out_of_range(ug):
     assert torch.equal(da[ok], a[ordenado[ok].long()]) and torch.equal(db[ok], b[ordenado[ok].long()])
 
 
-def _density_case(ug, oracle_lib, rows, dims, origin, cs, h):
+def _density_case(ug, oracle_lib, rows, dims, origin, cs, h, order=0):
     """GPU density through both access paths against the float64 oracle.
 
     Tolerance: each term's fp32 error is at most a few ulps of h^2 inside
@@ -90,9 +90,9 @@ def _density_case(ug, oracle_lib, rows, dims, origin, cs, h):
     (~100 * 2^-24 relative) that stays below 1e-4 * (rho + m_max h^6).  Terms
     whose inclusion fp32 and float64 decide differently have r^2 within a few
     ulps of h^2 and are ~1e-19 m h^6."""
-    got = gpu_build(ug, rows, dims, origin, cs)
     n = rows.shape[0]
-    p = ug.make_params(n, dims, origin, cs)
+    p = ug.make_params(n, dims, origin, cs, order=order)
+    got = gpu_build(ug, rows, dims, origin, cs, params=p)
     ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
     inicios = torch.from_numpy(got["inicios"].view(np.int32)).cuda()
     ordenado = torch.from_numpy(got["ordenado"].view(np.int32)).cuda()
@@ -103,7 +103,7 @@ def _density_case(ug, oracle_lib, rows, dims, origin, cs, h):
     assert ug.grid_status(ws) == 0
     a, b = rho_sorted.cpu().numpy(), rho_indirect.cpu().numpy()
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), "both paths add the same terms in the same order"
-    ref = oracle_lib.density(rows, dims, origin, cs, got["inicios"], got["ordenado"], h)
+    ref = oracle_lib.density(rows, dims, origin, cs, got["inicios"], got["ordenado"], h, order=order)
     by_particle = np.empty(n, np.float64)
     by_particle[got["ordenado"]] = a
     scale = float(rows[:, 7].max()) * float(h) ** 6 if n else 0.0

@@ -53,12 +53,33 @@ bool check_params(const grid_params *p, Geometry *g) {
     if (!std::isfinite(p->cellSize) || !(p->cellSize > 0.0f)) return false;
     const float inv = 1.0f / p->cellSize;  // fp32, rounded to nearest, once
     if (!std::isfinite(inv)) return false;
+    uint32_t bits[3] = {0u, 0u, 0u};
+    if (p->order == GRID_ORDER_MORTON) {
+        for (int d = 0; d < 3; ++d) {
+            if ((p->dims[d] & (p->dims[d] - 1u)) != 0u) return false;  // power of two
+            while ((1u << bits[d]) < p->dims[d]) ++bits[d];
+        }
+    } else if (p->order != GRID_ORDER_LINEAR) {
+        return false;
+    }
     if (g != nullptr) {
         for (int d = 0; d < 3; ++d) {
             g->origin[d] = p->origin[d];
             g->dims[d] = p->dims[d];
+            g->mask[d] = 0u;
         }
         g->inv_cell = inv;
+        g->order = kOrderLinear;
+        if (p->order == GRID_ORDER_MORTON) {
+            // Walk the levels as the Z-curve lays them out and note which code
+            // bit each axis's bit l lands on.
+            uint32_t pos = 0u;
+            for (uint32_t l = 0; l < 32u; ++l)
+                for (int d = 0; d < 3; ++d)
+                    if (l < bits[d]) g->mask[d] |= 1u << pos++;
+            const bool cubic = bits[0] == bits[1] && bits[1] == bits[2] && bits[0] <= 10u;
+            g->order = cubic ? kOrderMortonCubic : kOrderMorton;
+        }
     }
     return true;
 }

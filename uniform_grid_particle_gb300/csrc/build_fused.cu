@@ -18,7 +18,13 @@
 //           counters; the last CTA writes inicios[C] = N
 //                                                     ("Del conteo al inicio")
 //   scatter ordenado[inicios[c] + slots[i]] = i        ("La dispersión")
-//   gather  destino[k] = origen[ordenado[k]]   ("El kernel de reordenación")
+//           and, in the same pass, destino[inicios[c] + slots[i]] = origen[i]
+//
+// The last line is the pages' gather destino[k] = origen[ordenado[k]] ("El
+// kernel de reordenación") applied from the other side: the same permutation
+// gives the same destino, and the phase, its barrier and the re-read of
+// ordenado disappear.  Stable mode keeps a separate gather, because its
+// places are known only once every cell's segment is sorted.
 //
 // Because the count's atomic already hands out the slot, the pages' second
 // clear and second atomic pass are not needed: conteos ends as the histogram,
@@ -40,8 +46,9 @@
 // equal range per CTA, so every CTA has the same work in every phase.
 //
 // The count reads each record's first 16 bytes with an L2 evict-last policy
-// and the gather reads the records with evict-first: the 32-byte sectors the
-// count brings into L2 are still there when the gather needs them.
+// and the record move (or the stable gather) reads the records with
+// evict-first: the 32-byte sectors the count brings into L2 are still there
+// when the records move.
 //
 // Grid barriers: a CTA arrives with a release add on a counter that only grows
 // during the launch and waits, with acquire loads, until it reaches the number
@@ -74,12 +81,16 @@ namespace {
 #ifndef UGRID_FUSED_GATHER_ITEMS
 #define UGRID_FUSED_GATHER_ITEMS 4
 #endif
+#ifndef UGRID_FUSED_MOVE_ITEMS
+#define UGRID_FUSED_MOVE_ITEMS 4
+#endif
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCountItems = UGRID_FUSED_COUNT_ITEMS;      // particles per thread per round
 constexpr int kScatterItems = UGRID_FUSED_SCATTER_ITEMS;  // particles per thread per round
 constexpr int kGatherItems = UGRID_FUSED_GATHER_ITEMS;    // half-records per thread per round
+constexpr int kMoveItems = UGRID_FUSED_MOVE_ITEMS;        // half-records per thread per round
 constexpr int kScanVecs = 4;  // 16-byte vectors of counts a thread keeps between the scan phases
 constexpr int kAggBits = 11;  // the count's per-CTA grouping table: 2^11 entries
 constexpr int kAggSlots = 1 << kAggBits;
@@ -410,93 +421,137 @@ build_fused_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ destino
         hdr->counts_clean = (uint32_t)cells;
 
     UGRID_PHASE_MARK(4);
-    // ---- scatter: every particle to its slot ----------------------------------
-    for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
-        uint32_t cell[kScatterItems], slot[kScatterItems], start[kScatterItems];
+    if constexpr (!kStable) {
+        // ---- scatter with the records: ordenado and destino in one pass -----
+        // Particle i's place k = inicios[c] + slots[i] is known here, so its
+        // record goes straight to destino[k] instead of being fetched back
+        // through ordenado[k] after another grid barrier.  Two threads carry
+        // one record (a 16-byte half each), so every pair writes one whole
+        // 32-byte sector; the reads of origen are coalesced and hit the
+        // sectors the count kept in L2.
+        unsigned long long last_use;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(last_use));
+        const uint64_t h_lo = 2 * p_lo, h_hi = 2 * p_hi;
+        for (uint64_t r0 = h_lo; r0 < h_hi; r0 += (uint64_t)kThreads * kMoveItems) {
+            uint32_t cell[kMoveItems], slot[kMoveItems], start[kMoveItems];
+            uint4 v[kMoveItems];
 #pragma unroll
-        for (int k = 0; k < kScatterItems; ++k) {
-            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            if (i < p_hi) {
-                cell[k] = celdaDe[i];
-                slot[k] = slots[i];
+            for (int k = 0; k < kMoveItems; ++k) {
+                const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+                if (h < h_hi) {
+                    cell[k] = celdaDe[h >> 1];
+                    slot[k] = slots[h >> 1];
+                    v[k] = load_policy(origen + h, last_use);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kMoveItems; ++k) {
+                const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+                if (h < h_hi) start[k] = inicios[cell[k]];
+            }
+#pragma unroll
+            for (int k = 0; k < kMoveItems; ++k) {
+                const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+                if (h < h_hi) {
+                    const uint32_t pos = start[k] + slot[k];
+                    if (pos < n) {
+                        store_cs(destino + 2 * (uint64_t)pos + (h & 1), v[k]);
+                        if ((h & 1) == 0) ordenado[pos] = (uint32_t)(h >> 1);
+                    } else if ((h & 1) == 0) {
+                        record_status(&hdr->status, kStatusBounds);
+                    }
+                }
             }
         }
+    } else {
+        // ---- stable mode: scatter the indices, sort each cell, then gather -------
+        for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
+            uint32_t cell[kScatterItems], slot[kScatterItems], start[kScatterItems];
 #pragma unroll
-        for (int k = 0; k < kScatterItems; ++k) {
-            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            if (i < p_hi) start[k] = inicios[cell[k]];
-        }
+            for (int k = 0; k < kScatterItems; ++k) {
+                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+                if (i < p_hi) {
+                    cell[k] = celdaDe[i];
+                    slot[k] = slots[i];
+                }
+            }
 #pragma unroll
-        for (int k = 0; k < kScatterItems; ++k) {
-            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-            if (i < p_hi) {
-                const uint32_t pos = start[k] + slot[k];
-                if (pos < n)
-                    ordenado[pos] = (uint32_t)i;
-                else
-                    record_status(&hdr->status, kStatusBounds);
+            for (int k = 0; k < kScatterItems; ++k) {
+                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+                if (i < p_hi) start[k] = inicios[cell[k]];
+            }
+#pragma unroll
+            for (int k = 0; k < kScatterItems; ++k) {
+                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+                if (i < p_hi) {
+                    const uint32_t pos = start[k] + slot[k];
+                    if (pos < n)
+                        ordenado[pos] = (uint32_t)i;
+                    else
+                        record_status(&hdr->status, kStatusBounds);
+                }
             }
         }
-    }
-    UGRID_PHASE_END(4);
-    grid_barrier(hdr, passed);
-
-    if (kStable) {
-        // ---- stable mode: every cell's segment sorted by particle index ------
-        // ("Construir el índice…", §El orden dentro de la celda.)  Short
-        // segments are sorted by one thread in registers; longer ones are queued.
-        const uint64_t grid_threads = (uint64_t)ctas * kThreads;
-        for (uint64_t c = (uint64_t)blockIdx.x * kThreads + tid; c < cells; c += grid_threads) {
-            const uint32_t a = inicios[c];
-            if (!sort_short_segment(ordenado + a, inicios[c + 1] - a)) {
-                const uint32_t q = atomicAdd(&hdr->stable_big, 1u);
-                if (q < ws.queue_capacity)
-                    ws.queue[q] = (uint32_t)c;
-                else
-                    record_status(&hdr->status, kStatusBounds);
-            }
-        }
+        UGRID_PHASE_END(4);
         grid_barrier(hdr, passed);
-        // Long segments, one CTA each: bitonic in shared memory up to 8192
-        // indices, radix through the workspace scratch beyond.
-        const uint32_t queued = *reinterpret_cast<volatile uint32_t *>(&hdr->stable_big);
-        const uint32_t count = min(queued, ws.queue_capacity);
-        uint32_t *s_buf = reinterpret_cast<uint32_t *>(&s_held[0][0]);
-        for (uint32_t q = blockIdx.x; q < count; q += ctas) {
-            const uint32_t c = ws.queue[q];
-            const uint32_t a = inicios[c];
-            sort_long_segment<kThreads>(ordenado + a, ws.sort_scratch + a, inicios[c + 1] - a, n, s_buf,
-                                        kScanVecs * kThreads * 4);
-        }
-        grid_barrier(hdr, passed);
-    }
 
-    UGRID_PHASE_MARK(5);
-    // ---- gather: two threads per 32-byte record -------------------------------
-    unsigned long long last_use;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(last_use));
-    const uint64_t h_lo = 2 * p_lo, h_hi = 2 * p_hi;
-    for (uint64_t r0 = h_lo; r0 < h_hi; r0 += (uint64_t)kThreads * kGatherItems) {
-        uint32_t src[kGatherItems];
-#pragma unroll
-        for (int k = 0; k < kGatherItems; ++k) {
-            const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
-            src[k] = h < h_hi ? ordenado[h >> 1] : 0u;
+        {
+            // ---- every cell's segment sorted by particle index -------------------
+            // ("Construir el índice…", §El orden dentro de la celda.)  Short
+            // segments are sorted by one thread in registers; longer ones are queued.
+            const uint64_t grid_threads = (uint64_t)ctas * kThreads;
+            for (uint64_t c = (uint64_t)blockIdx.x * kThreads + tid; c < cells; c += grid_threads) {
+                const uint32_t a = inicios[c];
+                if (!sort_short_segment(ordenado + a, inicios[c + 1] - a)) {
+                    const uint32_t q = atomicAdd(&hdr->stable_big, 1u);
+                    if (q < ws.queue_capacity)
+                        ws.queue[q] = (uint32_t)c;
+                    else
+                        record_status(&hdr->status, kStatusBounds);
+                }
+            }
+            grid_barrier(hdr, passed);
+            // Long segments, one CTA each: bitonic in shared memory up to 8192
+            // indices, radix through the workspace scratch beyond.
+            const uint32_t queued = *reinterpret_cast<volatile uint32_t *>(&hdr->stable_big);
+            const uint32_t count = min(queued, ws.queue_capacity);
+            uint32_t *s_buf = reinterpret_cast<uint32_t *>(&s_held[0][0]);
+            for (uint32_t q = blockIdx.x; q < count; q += ctas) {
+                const uint32_t c = ws.queue[q];
+                const uint32_t a = inicios[c];
+                sort_long_segment<kThreads>(ordenado + a, ws.sort_scratch + a, inicios[c + 1] - a, n, s_buf,
+                                            kScanVecs * kThreads * 4);
+            }
+            grid_barrier(hdr, passed);
         }
-        uint4 v[kGatherItems];
+
+        UGRID_PHASE_MARK(5);
+        // ---- gather: two threads per 32-byte record -------------------------------
+        unsigned long long last_use;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(last_use));
+        const uint64_t h_lo = 2 * p_lo, h_hi = 2 * p_hi;
+        for (uint64_t r0 = h_lo; r0 < h_hi; r0 += (uint64_t)kThreads * kGatherItems) {
+            uint32_t src[kGatherItems];
 #pragma unroll
-        for (int k = 0; k < kGatherItems; ++k) {
-            const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
-            if (h < h_hi && src[k] < n) v[k] = load_policy(origen + 2 * (uint64_t)src[k] + (h & 1), last_use);
-        }
+            for (int k = 0; k < kGatherItems; ++k) {
+                const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+                src[k] = h < h_hi ? ordenado[h >> 1] : 0u;
+            }
+            uint4 v[kGatherItems];
 #pragma unroll
-        for (int k = 0; k < kGatherItems; ++k) {
-            const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
-            if (h < h_hi) {
-                if (src[k] < n)
-                    store_cs(destino + h, v[k]);
-                else if ((h & 1) == 0)
-                    record_status(&hdr->status, kStatusBounds);
+            for (int k = 0; k < kGatherItems; ++k) {
+                const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+                if (h < h_hi && src[k] < n) v[k] = load_policy(origen + 2 * (uint64_t)src[k] + (h & 1), last_use);
+            }
+#pragma unroll
+            for (int k = 0; k < kGatherItems; ++k) {
+                const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+                if (h < h_hi) {
+                    if (src[k] < n)
+                        store_cs(destino + h, v[k]);
+                    else if ((h & 1) == 0)
+                        record_status(&hdr->status, kStatusBounds);
+                }
             }
         }
     }

@@ -18,10 +18,19 @@ constexpr uint32_t kStatusBounds = 2u;
 constexpr unsigned long long kSpinLimitNs = 1000ull * 1000ull * 1000ull;
 
 // Grid geometry as the kernels see it (invCell already rounded on the host).
+// Cell orders as the kernels see them: the public GRID_ORDER_MORTON splits
+// into the cubic case (three equal sides, at most 2^10 each: a shift-and-mask
+// spread) and the general one (a bit deposit through per-axis masks).
+constexpr uint32_t kOrderLinear = 0u;
+constexpr uint32_t kOrderMorton = 1u;
+constexpr uint32_t kOrderMortonCubic = 2u;
+
 struct Geometry {
     float origin[3];
     float inv_cell;
     uint32_t dims[3];
+    uint32_t order;
+    uint32_t mask[3];  // Morton: the code bits each axis's bits go to, low to high
 };
 
 // ---- scan tiling --------------------------------------------------------
@@ -142,13 +151,39 @@ __device__ __forceinline__ uint32_t axis_coord(float p, float o, float inv, uint
     return f >= 0.0f ? min(__float2uint_rz(f), dim - 1u) : 0u;
 }
 
-// Linear cell index x + y*GX + z*GX*GY ("Reordenar por celda…", §El orden de
-// las celdas) of the position in the first 16 bytes of a record.
+// Bit i of the low ten bits of v moved to bit 3i (the classic halving spread:
+// each step moves the upper half of every group up by twice its distance).
+__device__ __forceinline__ uint32_t spread3(uint32_t v) {
+    v &= 0x3ffu;
+    v = (v | (v << 16)) & 0x030000ffu;
+    v = (v | (v << 8)) & 0x0300f00fu;
+    v = (v | (v << 4)) & 0x030c30c3u;
+    v = (v | (v << 2)) & 0x09249249u;
+    return v;
+}
+
+// The low bits of v placed, in order, at the set bits of mask.
+__device__ __forceinline__ uint32_t deposit(uint32_t v, uint32_t mask) {
+    uint32_t out = 0u;
+    for (uint32_t m = mask; m != 0u; m &= m - 1u, v >>= 1)
+        if (v & 1u) out |= m & (0u - m);
+    return out;
+}
+
+// Index of cell (x, y, z) in the grid's order ("Reordenar por celda…", §El
+// orden de las celdas): linear x + y*GX + z*GX*GY, or the Z-curve interleave.
+__device__ __forceinline__ uint32_t cell_at(uint32_t x, uint32_t y, uint32_t z, const Geometry &g) {
+    if (g.order == kOrderLinear) return x + g.dims[0] * (y + g.dims[1] * z);
+    if (g.order == kOrderMortonCubic) return spread3(x) | (spread3(y) << 1) | (spread3(z) << 2);
+    return deposit(x, g.mask[0]) | deposit(y, g.mask[1]) | deposit(z, g.mask[2]);
+}
+
+// Cell index of the position in the first 16 bytes of a record.
 __device__ __forceinline__ uint32_t cell_of(const uint4 &rec, const Geometry &g) {
     const uint32_t x = axis_coord(__uint_as_float(rec.x), g.origin[0], g.inv_cell, g.dims[0]);
     const uint32_t y = axis_coord(__uint_as_float(rec.y), g.origin[1], g.inv_cell, g.dims[1]);
     const uint32_t z = axis_coord(__uint_as_float(rec.z), g.origin[2], g.inv_cell, g.dims[2]);
-    return x + g.dims[0] * (y + g.dims[1] * z);
+    return cell_at(x, y, z, g);
 }
 
 // True (for the whole warp) when some valid lane holds the same key as the

@@ -28,8 +28,9 @@ contention      1,000,000   128^3      98 % N(0, 1)^3, 1 % on one cell centre
                                        [-8, 8)^3 (mostly outside: clamped);
                                        shuffled
 stress          16,777,216  256^3      uniform; built 10 times, ping-pong
-sph             1,000,000   36^3       uniform; ~90 neighbours within one cell
-                                       size, for the neighbour query
+sph             5,242,880   64^3       uniform; 20 per cell, ~84 neighbours
+                                       within one cell size, records (168 MB)
+                                       above L2: for the neighbour query
 =============== =========== ========== =========================================
 """
 from __future__ import annotations
@@ -96,9 +97,12 @@ SCENES: dict[str, Scene] = {
         Scene("headline", 1_000_000, (128, 128, 128), seed_index=2),
         Scene("contention", 1_000_000, (128, 128, 128), kind="contention", seed_index=3),
         Scene("stress", 16_777_216, (256, 256, 256), builds=10, seed_index=4),
-        # about 21 particles per cell and 90 within one cell size: the SPH-like
-        # neighbour count of "Reordenar por celda…" (§Qué cuesta la indirección)
-        Scene("sph", 1_000_000, (36, 36, 36), seed_index=5),
+        # 20 particles per cell, so about 84 within one cell size: the cell
+        # occupancy of "Contar partículas por celda" (§Elegir bien el tamaño de
+        # celda) and the SPH neighbour count of "Reordenar por celda…" (§Qué
+        # cuesta la indirección).  Power-of-two sides, so it also builds in
+        # Morton order.
+        Scene("sph", 5_242_880, (64, 64, 64), seed_index=5),
     )
 }
 

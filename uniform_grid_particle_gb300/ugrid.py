@@ -42,7 +42,12 @@ class grid_params(ctypes.Structure):
         ("dims", ctypes.c_uint32 * 3),
         ("origin", ctypes.c_float * 3),
         ("cellSize", ctypes.c_float),
+        ("order", ctypes.c_uint32),
     ]
+
+
+GRID_ORDER_LINEAR = 0
+GRID_ORDER_MORTON = 1
 
 
 class grid_array(ctypes.Structure):
@@ -51,8 +56,9 @@ class grid_array(ctypes.Structure):
     _fields_ = [("origen", ctypes.c_void_p), ("destino", ctypes.c_void_p), ("record_bytes", ctypes.c_uint32)]
 
 
-def make_params(n: int, dims, origin, cell_size: float) -> grid_params:
+def make_params(n: int, dims, origin, cell_size: float, order: int = GRID_ORDER_LINEAR) -> grid_params:
     p = grid_params()
+    p.order = int(order)
     p.conteo = int(n)
     p.dims[:] = [int(d) for d in dims]
     p.celdas = int(dims[0]) * int(dims[1]) * int(dims[2]) & 0xFFFFFFFF
