@@ -111,7 +111,8 @@ typedef struct grid_ws_header {
     uint32_t bar_count;    /* grid-barrier arrivals of the running fused build; 0 between calls */
     uint32_t bar_exit;     /* CTAs that finished the running fused build; 0 between calls */
     uint32_t counts_clean; /* cells of the fused build's counter array known to be zero */
-    uint32_t reserved[56];
+    uint32_t buckets_clean; /* 1 when the bucketed build's per-bucket totals are all zero */
+    uint32_t reserved[55];
 } grid_ws_header;
 
 /* Bytes of device workspace the calls below need for these params and flags

@@ -44,9 +44,12 @@ def test_workspace_bytes(L):
     tiles = (128 ** 3 + 8191) // 8192       # scan tiles of 8192 cells
     r256 = lambda b: (b + 255) // 256 * 256                     # noqa: E731
     # header, look-back words, per-CTA chunk sums (up to 4096 CTAs), per-particle slots,
-    # per-cell counters of the fused build
+    # per-cell counters of the fused build; then the bucketed build's tables
+    # (totals of up to 8192 buckets in 8 lanes each, bucket
+    # bases) and its (cell, particle) pairs
     assert L.grid_workspace_bytes(p, 0) == (256 + r256(tiles * 8) + r256(4096 * 4) + r256(4 * 1_000_000)
-                                            + r256(4 * 128 ** 3))
+                                            + r256(4 * 128 ** 3) + r256(4 * 8 * 8192) + r256(4 * 8192)
+                                            + r256(8 * 1_000_000))
     stable = L.grid_workspace_bytes(p, L.GRID_STABLE)
     assert stable >= L.grid_workspace_bytes(p, 0) + 4 * 1_000_000
     assert L.grid_workspace_bytes(p, 2) == 0            # unknown flag

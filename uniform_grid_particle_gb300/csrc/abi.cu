@@ -21,6 +21,14 @@ WsLayout ws_layout(uint64_t n, uint64_t cells, unsigned flags) {
     off = round_up(off + n * sizeof(uint32_t), 256);
     l.counts = off;
     off = round_up(off + cells * sizeof(uint32_t), 256);
+    if (n != 0) {
+        l.bucket_total = off;
+        off = round_up(off + kBucketMaxCount * kBucketLanes * sizeof(uint32_t), 256);
+        l.bucket_base = off;
+        off = round_up(off + kBucketMaxCount * sizeof(uint32_t), 256);
+        l.pairs = off;
+        off = round_up(off + n * 2 * sizeof(uint32_t), 256);
+    }
     if (flags & GRID_STABLE) {
         l.stable_queue = off;
         off = round_up(off + segment_queue_capacity(n, cells) * sizeof(uint32_t), 256);
@@ -226,6 +234,17 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     grid_ws_header *h = header(ws);
     char *base = static_cast<char *>(ws);
+    if ((flags & GRID_STABLE) == 0 && n != 0) {
+        // The two-level counting sort in one cooperative launch (build_bucketed.cu).
+        const cudaError_t f = launch_build_bucketed(
+            origen, destino, conteos, celdaDe, inicios, ordenado, p->conteo, c, g, h,
+            reinterpret_cast<uint32_t *>(base + l.chunk_sums), reinterpret_cast<uint32_t *>(base + l.slots),
+            reinterpret_cast<uint32_t *>(base + l.counts), reinterpret_cast<uint32_t *>(base + l.bucket_total),
+            reinterpret_cast<uint32_t *>(base + l.bucket_base),
+            reinterpret_cast<uint32_t *>(base + l.pairs), st);
+        if (f != cudaErrorNotSupported) return cuda_code(f);
+        (void)cudaGetLastError();
+    }
     {
         // The whole chain in one cooperative launch (build_fused.cu).
         const bool stable = (flags & GRID_STABLE) != 0;

@@ -1,0 +1,462 @@
+// The grid build as a two-level counting sort, in one cooperative launch.
+//
+// The pages count with one global atomic per particle ("Contar partículas por
+// celda", §El kernel).  With about one particle per cell nothing can be
+// grouped, and the L2 atomic units become the limit of the whole build.  This
+// build reaches the same outputs with atomics in shared memory only, by first
+// sorting the particles into buckets of 2^shift consecutive cells (the
+// leading bits of the cell index, as in the first pass of an MSD radix sort):
+//
+//   A  cells: celdaDe[i] = cell of particle i; each CTA histograms its
+//      particles over the buckets in shared memory and adds its histogram to
+//      the bucket totals, one global atomic per CTA and bucket, whose old
+//      value is where the CTA's stretch of the bucket starts
+//   C  bucket bases = exclusive scan of the totals; each CTA sends its
+//      particles to its stretches as (cell, particle) pairs
+//
+// A bucket's total is kBucketLanes words, CTA j adding to lane
+// j mod kBucketLanes: a word then takes the atomics of only
+// ctas / kBucketLanes CTAs (atomics on one word are serialised in L2).  Lane
+// r's part of a bucket starts after the totals of lanes 0..r-1.
+//   D  per bucket, one CTA: a shared-memory histogram over the bucket's cells
+//      gives conteos and, scanned from the bucket's base, inicios ("Construir
+//      el índice de la rejilla con un prefix sum", §Del conteo al inicio);
+//      the slot each particle took in its cell's counter places it
+//      (§La dispersión), and the bucket's stretch of ordenado and destino is
+//      written in order ("Reordenar por celda…", §El kernel de reordenación:
+//      destino[k] = origen[ordenado[k]])
+//
+// The buckets are `width` consecutive cells (a multiple of 4, so bucket
+// boundaries keep 16-byte alignment); the bucket of cell c is c / width,
+// taken as the high word of c * ceil(2^64 / width), exact for every 32-bit c
+// because c * (ceil(2^64 / width) * width - 2^64) < 2^32 * width < 2^64.
+// The plan makes the bucket count a multiple of the CTA count, so in a
+// uniform scene every CTA places the same number of buckets.
+//
+// The totals are zero between builds: the CTA that places a bucket zeroes its
+// words, and a header word records that all of them are clean (a build that
+// did not finish leaves it unset and the next one clears them first).
+//
+// Every output is one the pages' chain can produce: conteos and inicios are
+// the histogram and its exclusive scan, and each cell's segment of ordenado
+// holds exactly its particles (in shared-memory arrival order).
+//
+// A bucket of more than kBucketCap particles would not fit one CTA's shared
+// memory.  Every CTA sees the same totals, so all of them then take the
+// atomic path of the fused build instead (count from celdaDe, scan, scatter
+// with the records), and the result is the same.
+//
+// Phases A and C read a CTA's contiguous range of particles, phase D takes
+// buckets cyclically, and grid barriers separate the phases (see
+// fused_common.cuh: bounded waits that record kStatusTimeout).
+#include <atomic>
+
+#include "fused_common.cuh"
+
+namespace ugrid {
+namespace {
+
+using namespace fused;
+
+constexpr int kBucketItems = (int)(kBucketCap / kThreads);  // particles per thread in phase D
+static_assert(kBucketItems * kThreads == (int)kBucketCap, "phase D holds a whole bucket in registers");
+static_assert(kBucketMaxCells == kScanVecs * 4 * kThreads && kBucketMaxCount == kScanVecs * 4 * kThreads,
+              "bucket tables are the 32 KB scan table");
+constexpr size_t kTableBytes = (size_t)kScanVecs * kThreads * sizeof(uint4);  // 32 KB
+constexpr size_t kDynamicSmem = kTableBytes + 3 * kBucketCap * sizeof(uint32_t);  // + 3 x 16 KB buffers
+constexpr int kMaxDevices = 64;
+
+struct BucketScratch {
+    uint32_t width;              // cells per bucket
+    uint32_t buckets;            // B
+    unsigned long long magic;    // ceil(2^64 / width)
+    uint32_t *total;             // [B][kBucketLanes] particles per bucket and lane, zero between builds
+    uint32_t *base;              // [B] first position of each bucket
+    uint2 *pairs;                // [n] (cell, particle), grouped by bucket
+};
+
+
+
+__device__ __forceinline__ uint32_t bucket_of(uint32_t c, const BucketScratch &bk) {
+    return (uint32_t)__umul64hi((unsigned long long)c, bk.magic);
+}
+
+static_assert(kBucketLanes == 8, "a bucket's lane words are two 16-byte vectors");
+
+// Particles of bucket b (all lanes) and, in `before`, those of lanes below r.
+__device__ __forceinline__ uint32_t bucket_total(const uint32_t *total, uint32_t b, uint32_t r, uint32_t &before) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(total + (uint64_t)b * kBucketLanes);
+    const uint4 lo = p[0], hi = p[1];
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t sum = 0, pre = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        pre += (uint32_t)e < r ? w[e] : 0u;
+        sum += w[e];
+    }
+    before = pre;
+    return sum;
+}
+
+__device__ __forceinline__ void zero_bucket(uint32_t *total, uint32_t b) {
+    uint4 *t = reinterpret_cast<uint4 *>(total + (uint64_t)b * kBucketLanes);
+    t[0] = t[1] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Shared-memory add of 1 to table[key] for every valid lane; returns the
+// value before this lane's add.  Lanes of a warp that share a key are served
+// by one atomic of their leader when the cheap adjacent-duplicate test finds
+// any, so crowded keys do not serialise.
+__device__ __forceinline__ uint32_t smem_take(uint32_t *table, bool valid, uint32_t key) {
+    if (warp_has_adjacent_duplicates(valid, key)) {
+        const uint32_t active = __ballot_sync(0xffffffffu, valid);
+        uint32_t first = 0u, peers = 0u;
+        if (valid) {
+            peers = __match_any_sync(active, key);
+            const uint32_t leader = (uint32_t)(__ffs(peers) - 1);
+            if (lane_id() == leader) first = atomicAdd(&table[key], (uint32_t)__popc(peers));
+            first = __shfl_sync(peers, first, leader);
+        }
+        return first + (uint32_t)__popc(peers & lanemask_lt());
+    }
+    return valid ? atomicAdd(&table[key], 1u) : 0u;
+}
+
+// A bucket too large for one CTA: every CTA takes the atomic path of the
+// fused build from celdaDe on.  Kept out of line so that its registers do not
+// weigh on the bucketed phases.
+__device__ __noinline__ void atomic_path(const BuildArgs a, const Geometry g, grid_ws_header *hdr,
+                                         const FusedScratch ws, const BucketScratch bk, bool clean,
+                                         uint32_t &passed, uint64_t p_lo, uint64_t p_hi, uint4 (*s_held)[kThreads],
+                                         uint32_t *s_red, uint32_t (*s_rows)[kWarps]) {
+    if (!clean) {
+        clear_counters(ws.counts, a.cells);
+        grid_barrier(hdr, passed);
+    }
+    count_phase<false>(a, g, ws, p_lo, p_hi, s_held);
+    grid_barrier(hdr, passed);
+    if (blockIdx.x == 0 && threadIdx.x == 0) hdr->counts_clean = 0u;
+    // Every CTA has read the bucket totals by now: clear them for the next build.
+    for (uint32_t b = blockIdx.x * kThreads + threadIdx.x; b < bk.buckets; b += gridDim.x * kThreads)
+        zero_bucket(bk.total, b);
+    const ScanChunk chunk = scan_chunk(a.cells);
+    scan_totals_phase(ws, chunk, s_held, s_red);
+    grid_barrier(hdr, passed);
+    scan_starts_phase(a, ws, chunk, s_held, s_red, s_rows);
+    grid_barrier(hdr, passed);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && (hdr->status & kStatusTimeout) == 0)
+        hdr->counts_clean = (uint32_t)a.cells;
+    scatter_move_phase(a, ws, &hdr->status, p_lo, p_hi);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch ws, BucketScratch bk) {
+    extern __shared__ uint4 s_dyn[];
+    uint4(*s_held)[kThreads] = reinterpret_cast<uint4(*)[kThreads]>(s_dyn);
+    uint32_t *s_table = reinterpret_cast<uint32_t *>(s_dyn);                        // u32[8192], same bytes
+    uint32_t *s_order = reinterpret_cast<uint32_t *>(s_dyn + kScanVecs * kThreads);  // u32[kBucketCap]
+    uint32_t *s_who = s_order + kBucketCap;                                           // u32[kBucketCap]
+    uint32_t *s_place = s_who + kBucketCap;                                           // u32[kBucketCap]
+    __shared__ uint32_t s_red[kWarps];
+    __shared__ uint32_t s_rows[kScanVecs][kWarps];
+    __shared__ uint32_t s_clean, s_bclean, s_base, s_count;
+    const uint32_t tid = threadIdx.x;
+    const uint32_t ctas = gridDim.x;
+    const uint32_t B = bk.buckets;
+    uint32_t passed = 0;
+    if (tid == 0) {
+        s_clean = *reinterpret_cast<volatile uint32_t *>(&hdr->counts_clean) >= a.cells;
+        s_bclean = *reinterpret_cast<volatile uint32_t *>(&hdr->buckets_clean) != 0u;
+    }
+    for (uint32_t b = tid; b < kBucketMaxCount; b += kThreads) s_table[b] = 0u;
+    __syncthreads();
+    uint64_t p_lo, p_hi;
+    particle_range(a.n, p_lo, p_hi);
+
+    UGRID_PHASE_MARK(0);
+    if (!s_bclean) {
+        for (uint32_t b = blockIdx.x * kThreads + tid; b < B; b += ctas * kThreads) zero_bucket(bk.total, b);
+        grid_barrier(hdr, passed);
+    }
+
+    // ---- A: cells and the bucket totals ------------------------------------------
+    UGRID_PHASE_MARK(1);
+    {
+        unsigned long long keep;
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+        for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kCountItems) {
+            uint4 rec[kCountItems];
+#pragma unroll
+            for (int k = 0; k < kCountItems; ++k) {
+                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+                if (i < p_hi) rec[k] = load_policy(a.origen + 2 * i, keep);
+            }
+#pragma unroll
+            for (int k = 0; k < kCountItems; ++k) {
+                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+                const bool valid = i < p_hi;
+                uint32_t bucket = 0u;
+                if (valid) {
+                    const uint32_t c = cell_of(rec[k], g);
+                    a.celdaDe[i] = c;
+                    bucket = bucket_of(c, bk);
+                }
+                smem_take(s_table, valid, bucket);
+            }
+        }
+    }
+    __syncthreads();
+    // This CTA's stretch within its lane of every bucket it has particles in:
+    // the atomic's old value is the offset, and the lane words end as totals.
+    for (uint32_t b = tid; b < B; b += kThreads) {
+        const uint32_t m = s_table[b];
+        if (m) s_table[b] = atomicAdd(bk.total + (uint64_t)b * kBucketLanes + blockIdx.x % kBucketLanes, m);
+    }
+    UGRID_PHASE_END(1);
+    grid_barrier(hdr, passed);
+    if (blockIdx.x == 0 && tid == 0) hdr->buckets_clean = 0u;
+
+    // ---- C: bucket bases, this CTA's stretch of each bucket, the pairs ------------
+    UGRID_PHASE_MARK(3);
+    bool heavy;
+    {
+        const uint32_t lane_r = blockIdx.x % kBucketLanes;
+        uint32_t *s_start = s_order;  // u32[kBucketMaxCount]: s_order and s_who are free until phase D
+        uint4 v[kScanVecs];
+        uint32_t t[kScanVecs], most = 0;
+#pragma unroll
+        for (int q = 0; q < kScanVecs; ++q) {
+            const uint32_t b0 = 4u * (q * kThreads + tid);
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                w[e] = 0u;
+                if (b0 + e < B) {
+                    uint32_t before;
+                    w[e] = bucket_total(bk.total, b0 + e, lane_r, before);
+                    s_start[b0 + e] = before;
+                }
+            }
+            v[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            t[q] = v[q].x + v[q].y + v[q].z + v[q].w;
+            most = max(most, max(max(v[q].x, v[q].y), max(v[q].z, v[q].w)));
+        }
+        most = __reduce_max_sync(0xffffffffu, most);
+        if (lane_id() == 0) s_red[tid >> 5] = most;
+        uint32_t excl[kScanVecs], rows[kScanVecs];
+        rows_exclusive_scan(t, excl, rows, s_rows);  // its barriers also publish s_red
+        most = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) most = max(most, s_red[w]);
+        heavy = most > kBucketCap;
+        if (!heavy) {
+            uint32_t row_base = 0;
+#pragma unroll
+            for (int q = 0; q < kScanVecs; ++q) {
+                const uint32_t b0 = 4u * (q * kThreads + tid);
+                const uint32_t f = row_base + excl[q];
+                const uint32_t start[4] = {f, f + v[q].x, f + v[q].x + v[q].y, f + v[q].x + v[q].y + v[q].z};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (b0 + e < B) {
+                        if (blockIdx.x == 0) bk.base[b0 + e] = start[e];
+                        s_table[b0 + e] += s_start[b0 + e] + start[e];  // cursor of this CTA's stretch
+                    }
+                }
+                row_base += rows[q];
+            }
+        }
+    }
+    __syncthreads();
+
+    UGRID_PHASE_MARK(2);
+    if (heavy) {
+        atomic_path(a, g, hdr, ws, bk, s_clean != 0u, passed, p_lo, p_hi, s_held, s_red, s_rows);
+    } else {
+        for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
+            uint32_t cell[kScatterItems];
+#pragma unroll
+            for (int k = 0; k < kScatterItems; ++k) {
+                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+                if (i < p_hi) cell[k] = a.celdaDe[i];
+            }
+#pragma unroll
+            for (int k = 0; k < kScatterItems; ++k) {
+                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+                const bool valid = i < p_hi;
+                const uint32_t q = smem_take(s_table, valid, valid ? bucket_of(cell[k], bk) : 0u);
+                if (valid) {
+                    if (q < a.n)
+                        bk.pairs[q] = make_uint2(cell[k], (uint32_t)i);
+                    else
+                        record_status(&hdr->status, kStatusBounds);
+                }
+            }
+        }
+        UGRID_PHASE_END(3);
+        grid_barrier(hdr, passed);
+
+        // ---- D: each bucket placed by one CTA ---------------------------------
+        UGRID_PHASE_MARK(4);
+        for (uint32_t b = blockIdx.x; b < B; b += ctas) {
+            const uint64_t cl = (uint64_t)b * bk.width;
+            const uint32_t w = (uint32_t)min((uint64_t)bk.width, a.cells - cl);
+            if (tid == 0) {
+                s_base = bk.base[b];
+                uint32_t unused;
+                s_count = bucket_total(bk.total, b, 0u, unused);
+                zero_bucket(bk.total, b);  // clean for the next build
+            }
+#pragma unroll
+            for (int q = 0; q < kScanVecs; ++q) s_held[q][tid] = make_uint4(0u, 0u, 0u, 0u);
+            __syncthreads();
+            const uint32_t base = s_base;
+            const uint32_t t = base <= a.n ? min(min(s_count, kBucketCap), a.n - base) : 0u;
+            // (cell within the bucket) << 16 | slot within the cell; ~0u for none
+#pragma unroll
+            for (int k = 0; k < kBucketItems; ++k) {
+                const uint32_t q = (uint32_t)k * kThreads + tid;
+                bool valid = q < t;
+                uint32_t local = 0u;
+                if (valid) {
+                    const uint2 pr = bk.pairs[base + q];
+                    local = pr.x - (uint32_t)cl;
+                    s_who[q] = pr.y;
+                    if (local >= w) {
+                        record_status(&hdr->status, kStatusBounds);
+                        valid = false;
+                    }
+                }
+                const uint32_t slot = smem_take(s_table, valid, valid ? local : 0u);
+                if (q < t) s_place[q] = valid ? (local << 16) | slot : 0xffffffffu;
+            }
+            __syncthreads();
+            {
+                uint4 v[kScanVecs];
+                uint32_t tt[kScanVecs], excl[kScanVecs], rows[kScanVecs];
+#pragma unroll
+                for (int q = 0; q < kScanVecs; ++q) {
+                    v[q] = s_held[q][tid];
+                    tt[q] = v[q].x + v[q].y + v[q].z + v[q].w;
+                }
+                rows_exclusive_scan(tt, excl, rows, s_rows);
+                uint32_t row_base = base;
+#pragma unroll
+                for (int q = 0; q < kScanVecs; ++q) {
+                    const uint64_t l = 4ull * (q * kThreads + tid);
+                    const uint32_t f = row_base + excl[q];
+                    store_starts(a.inicios + cl, l, w, f, v[q]);
+                    if (l + 4 <= w) {
+                        *reinterpret_cast<uint4 *>(a.conteos + cl + l) = v[q];
+                    } else {
+                        const uint32_t c3[3] = {v[q].x, v[q].y, v[q].z};
+                        for (int e = 0; e < 3; ++e)
+                            if (l + e < w) a.conteos[cl + l + e] = c3[e];
+                    }
+                    s_held[q][tid] = make_uint4(f, f + v[q].x, f + v[q].x + v[q].y, f + v[q].x + v[q].y + v[q].z);
+                    row_base += rows[q];
+                }
+            }
+            __syncthreads();
+            UGRID_PHASE_MARK(5);
+            for (uint32_t q = tid; q < t; q += kThreads) {
+                const uint32_t place = s_place[q];
+                if (place != 0xffffffffu) {
+                    const uint32_t at = s_table[place >> 16] + (place & 0xffffu) - base;
+                    if (at < t)
+                        s_order[at] = s_who[q];
+                    else
+                        record_status(&hdr->status, kStatusBounds);
+                }
+            }
+            __syncthreads();
+            UGRID_PHASE_MARK(7);
+            for (uint32_t q = tid; q < t; q += kThreads) a.ordenado[base + q] = s_order[q];
+            // The bucket's records, gathered in order ("El kernel de
+            // reordenación": destino[k] = origen[ordenado[k]]).
+            unsigned long long last_use;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(last_use));
+            for (uint32_t h0 = 0; h0 < 2 * t; h0 += kThreads * kGatherItems) {
+                uint32_t src[kGatherItems];
+                uint4 rec[kGatherItems];
+#pragma unroll
+                for (int k = 0; k < kGatherItems; ++k) {
+                    const uint32_t h = h0 + (uint32_t)k * kThreads + tid;
+                    src[k] = h < 2 * t ? s_order[h >> 1] : a.n;
+                    if (src[k] < a.n) rec[k] = load_policy(a.origen + 2 * (uint64_t)src[k] + (h & 1), last_use);
+                }
+#pragma unroll
+                for (int k = 0; k < kGatherItems; ++k) {
+                    const uint32_t h = h0 + (uint32_t)k * kThreads + tid;
+                    if (src[k] < a.n) store_cs(a.destino + 2 * (uint64_t)base + h, rec[k]);
+                }
+            }
+            __syncthreads();  // the tables are cleared for the next bucket
+        }
+        if (blockIdx.x == 0 && tid == 0) a.inicios[a.cells] = a.n;
+    }
+    UGRID_PHASE_MARK(6);
+    // The last CTA out: every bucket word has been zeroed.
+    if (tid == 0 && atomicAdd(&hdr->bar_exit, 1u) == ctas - 1u) {
+        if ((hdr->status & kStatusTimeout) == 0) hdr->buckets_clean = 1u;
+        hdr->bar_count = 0u;
+        hdr->bar_exit = 0u;
+    }
+}
+
+std::atomic<int> g_grid[kMaxDevices];  // cached grid size per device (0 = not yet known)
+
+cudaError_t bucketed_grid(int device, int *grid) {
+    if (device >= 0 && device < kMaxDevices) {
+        const int cached = g_grid[device].load(std::memory_order_relaxed);
+        if (cached != 0) {
+            *grid = cached;
+            return cached > 0 ? cudaSuccess : cudaErrorNotSupported;
+        }
+    }
+    int coop = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaFuncSetAttribute(build_bucketed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kDynamicSmem);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_bucketed_kernel, kThreads, kDynamicSmem);
+    if (e != cudaSuccess) return e;
+    int gsz = coop ? per_sm * sms : -1;
+    if (gsz <= 0 || gsz > (int)kFusedMaxCtas) gsz = -1;
+    if (device >= 0 && device < kMaxDevices) g_grid[device].store(gsz, std::memory_order_relaxed);
+    *grid = gsz;
+    return gsz > 0 ? cudaSuccess : cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_build_bucketed(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
+                                  uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, uint32_t n,
+                                  uint64_t cells, const Geometry &g, grid_ws_header *hdr, uint32_t *chunk_sums,
+                                  uint32_t *slots, uint32_t *counts, uint32_t *total, uint32_t *base,
+                                  uint32_t *pairs, cudaStream_t s) {
+    int device = 0, grid = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e == cudaSuccess) e = bucketed_grid(device, &grid);
+    if (e != cudaSuccess) return e;
+    const BucketPlan plan = bucket_plan(n, cells, (uint32_t)grid);
+    if (plan.buckets == 0) return cudaErrorNotSupported;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kDynamicSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const FusedScratch ws{chunk_sums, slots, counts, nullptr, 0u, nullptr};
+    const BucketScratch bk{plan.width, plan.buckets, plan.magic, total, base, reinterpret_cast<uint2 *>(pairs)};
+    const BuildArgs a{reinterpret_cast<const uint4 *>(origen), reinterpret_cast<uint4 *>(destino), conteos, celdaDe,
+                      inicios, ordenado, n, cells};
+    return cudaLaunchKernelEx(&cfg, build_bucketed_kernel, a, g, hdr, ws, bk);
+}
+
+}  // namespace ugrid

@@ -43,11 +43,47 @@ inline uint64_t scan_tiles(uint64_t cells) { return (cells + kScanTile - 1) / kS
 // ---- workspace layout ---------------------------------------------------
 constexpr size_t kHeaderBytes = 256;
 constexpr uint32_t kFusedMaxCtas = 4096;  // bound on the fused build's grid
+// The bucketed build groups the cells into buckets of `width` consecutive
+// cells.  A bucket's counters, and a CTA's counters of all buckets, each fill
+// one CTA's 32 KB table, so both are capped at 8192; a bucket holding more
+// than kBucketCap particles sends the whole build down the atomic path.
+constexpr uint32_t kBucketMaxCells = 8192;
+constexpr uint32_t kBucketMaxCount = 8192;
+constexpr uint32_t kBucketCap = 4096;   // particles one CTA places in shared memory
+constexpr uint32_t kBucketAvg = 3300;   // particles per bucket aimed at (uniform scenes stay far below the cap)
+constexpr uint32_t kBucketLanes = 8;    // counters per bucket, so that few CTAs add to the same word
+struct BucketPlan {
+    uint32_t width;              // cells per bucket, a multiple of 4
+    uint32_t buckets;            // 0: the bucketed build is not used
+    unsigned long long magic;    // ceil(2^64 / width): bucket = umulhi64(cell, magic)
+};
+// A whole number of buckets per CTA of the launch (`ctas`), each holding
+// about kBucketAvg particles of a uniform scene, with at most kBucketMaxCells
+// cells per bucket and kBucketMaxCount buckets.
+inline BucketPlan bucket_plan(uint64_t n, uint64_t cells, uint32_t ctas) {
+    BucketPlan p{0u, 0u, 0ull};
+    if (n == 0 || cells == 0 || ctas == 0) return p;
+    const uint64_t per_cta = (n + (uint64_t)ctas * kBucketAvg - 1) / ((uint64_t)ctas * kBucketAvg);
+    uint64_t b = (uint64_t)ctas * per_cta;
+    uint64_t w = (cells + b - 1) / b;
+    w = (w + 3) & ~3ull;
+    if (w > kBucketMaxCells) w = kBucketMaxCells;
+    b = (cells + w - 1) / w;
+    if (b > kBucketMaxCount) return p;
+    p.width = (uint32_t)w;
+    p.buckets = (uint32_t)b;
+    p.magic = ~0ull / w + 1ull;  // w >= 4, so this is ceil(2^64 / w)
+    return p;
+}
+
 struct WsLayout {
     size_t tile_status;     // u64[tiles]
     size_t chunk_sums;      // u32[kFusedMaxCtas] per-CTA cell-chunk totals (fused build)
     size_t slots;           // u32[n] slot of each particle in its cell (fused build)
     size_t counts;          // u32[cells] counters of the fused build, zero between builds
+    size_t bucket_total;    // u32[kBucketMaxCount][kBucketLanes] particles per bucket and lane, zero between builds
+    size_t bucket_base;     // u32[kBucketMaxCount] first position of each bucket
+    size_t pairs;           // u32x2[n] (cell, particle) grouped by bucket
     size_t stable_queue;    // u32[cells] queue of long segments (GRID_STABLE)
     size_t stable_scratch;  // u32[n] radix-sort scratch (GRID_STABLE)
     size_t total;
@@ -102,6 +138,11 @@ cudaError_t launch_build_fused(const ugrid_particula *origen, ugrid_particula *d
                                grid_ws_header *hdr, uint32_t *chunk_sums, uint32_t *slots,
                                uint32_t *counts, bool stable, uint32_t *queue,
                                uint32_t queue_capacity, uint32_t *sort_scratch, cudaStream_t s);
+cudaError_t launch_build_bucketed(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
+                                  uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, uint32_t n,
+                                  uint64_t cells, const Geometry &g, grid_ws_header *hdr, uint32_t *chunk_sums,
+                                  uint32_t *slots, uint32_t *counts, uint32_t *total, uint32_t *base,
+                                  uint32_t *pairs, cudaStream_t s);
 
 // Several arrays gathered with one ordenado (grid_reorder_many).
 constexpr int kMaxArrays = 4;
