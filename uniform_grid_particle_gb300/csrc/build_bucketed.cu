@@ -3,9 +3,10 @@
 // The pages count with one global atomic per particle ("Contar partículas por
 // celda", §El kernel).  With about one particle per cell nothing can be
 // grouped, and the L2 atomic units become the limit of the whole build.  This
-// build reaches the same outputs with atomics in shared memory only, by first
-// sorting the particles into buckets of 2^shift consecutive cells (the
-// leading bits of the cell index, as in the first pass of an MSD radix sort):
+// build reaches the same outputs with atomics in shared memory, plus one
+// global atomic per CTA and bucket, by first sorting the particles into
+// buckets of `width` consecutive cells (as in the first pass of an MSD radix
+// sort):
 //
 //   A  cells: celdaDe[i] = cell of particle i; each CTA histograms its
 //      particles over the buckets in shared memory and adds its histogram to
@@ -13,11 +14,6 @@
 //      value is where the CTA's stretch of the bucket starts
 //   C  bucket bases = exclusive scan of the totals; each CTA sends its
 //      particles to its stretches as (cell, particle) pairs
-//
-// A bucket's total is kBucketLanes words, CTA j adding to lane
-// j mod kBucketLanes: a word then takes the atomics of only
-// ctas / kBucketLanes CTAs (atomics on one word are serialised in L2).  Lane
-// r's part of a bucket starts after the totals of lanes 0..r-1.
 //   D  per bucket, one CTA: a shared-memory histogram over the bucket's cells
 //      gives conteos and, scanned from the bucket's base, inicios ("Construir
 //      el índice de la rejilla con un prefix sum", §Del conteo al inicio);
@@ -26,6 +22,10 @@
 //      written in order ("Reordenar por celda…", §El kernel de reordenación:
 //      destino[k] = origen[ordenado[k]])
 //
+// Every output is one the pages' chain can produce: conteos and inicios are
+// the histogram and its exclusive scan, and each cell's segment of ordenado
+// holds exactly its particles (in shared-memory arrival order).
+//
 // The buckets are `width` consecutive cells (a multiple of 4, so bucket
 // boundaries keep 16-byte alignment); the bucket of cell c is c / width,
 // taken as the high word of c * ceil(2^64 / width), exact for every 32-bit c
@@ -33,13 +33,13 @@
 // The plan makes the bucket count a multiple of the CTA count, so in a
 // uniform scene every CTA places the same number of buckets.
 //
-// The totals are zero between builds: the CTA that places a bucket zeroes its
-// words, and a header word records that all of them are clean (a build that
-// did not finish leaves it unset and the next one clears them first).
-//
-// Every output is one the pages' chain can produce: conteos and inicios are
-// the histogram and its exclusive scan, and each cell's segment of ordenado
-// holds exactly its particles (in shared-memory arrival order).
+// A bucket's total is kBucketLanes words, CTA j adding to lane
+// j mod kBucketLanes: a word then takes the atomics of only
+// ctas / kBucketLanes CTAs (atomics on one word are serialised in L2).  Lane
+// r's part of a bucket starts after the totals of lanes 0..r-1.  The totals
+// are zero between builds: the CTA that places a bucket zeroes its words, and
+// a header word records that all of them are clean (a build that did not
+// finish leaves it unset and the next one clears them first).
 //
 // A bucket of more than kBucketCap particles would not fit one CTA's shared
 // memory.  Every CTA sees the same totals, so all of them then take the
@@ -59,7 +59,7 @@ namespace {
 using namespace fused;
 
 constexpr int kBucketItems = (int)(kBucketCap / kThreads);  // particles per thread in phase D
-static_assert(kBucketItems * kThreads == (int)kBucketCap, "phase D holds a whole bucket in registers");
+static_assert(kBucketItems * kThreads == (int)kBucketCap, "phase D takes a whole bucket in one round");
 static_assert(kBucketMaxCells == kScanVecs * 4 * kThreads && kBucketMaxCount == kScanVecs * 4 * kThreads,
               "bucket tables are the 32 KB scan table");
 constexpr size_t kTableBytes = (size_t)kScanVecs * kThreads * sizeof(uint4);  // 32 KB
@@ -74,8 +74,6 @@ struct BucketScratch {
     uint32_t *base;              // [B] first position of each bucket
     uint2 *pairs;                // [n] (cell, particle), grouped by bucket
 };
-
-
 
 __device__ __forceinline__ uint32_t bucket_of(uint32_t c, const BucketScratch &bk) {
     return (uint32_t)__umul64hi((unsigned long long)c, bk.magic);
