@@ -72,18 +72,22 @@ def hbm_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_traffic(kernel_source: str) -> float | None:
+def kernel_traffic(sources: list[str]) -> float | None:
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of that kernel (sha256 of the .cu file)."""
+    on the current source of that kernel (sha256 over its source files, in
+    order, as named in the summary's first column joined by '+')."""
     try:
         lines = open(TRAFFIC_FILE).read().splitlines()
     except OSError:
         return None
-    src = os.path.join(ROOT, "uniform_grid_particle_gb300", "csrc", kernel_source)
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    h = hashlib.sha256()
+    for name in sources:
+        with open(os.path.join(ROOT, "uniform_grid_particle_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    key, digest = "+".join(sources), h.hexdigest()
     for line in lines:
         parts = line.split()
-        if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_source:
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == key:
             return float(parts[2]) if parts[1] == digest else None
     return None
 
@@ -239,16 +243,20 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# The kernel one non-stable grid_build launches (and the sources its DRAM
+# traffic is keyed by), and the one a stable build launches.
+BUILD_KERNEL = ("build_bucketed_kernel", ["build_bucketed.cu", "fused_common.cuh"])
+STABLE_KERNEL = ("build_fused_kernel<true>", ["build_fused.cu", "fused_common.cuh"])
+
+
 def roofline_entry(flags: int, total_alg: int, ms_per_step: float, peak: float, peak_kind: str) -> dict:
-    """The timed step is one launch of the fused build kernel (non-stable
-    builds): its algorithmic bytes are the whole build's, its duration the
-    step's event time."""
+    """The timed step is one launch of the build kernel: its algorithmic
+    bytes are the whole build's, its duration the step's event time."""
     achieved = total_alg / (ms_per_step * 1e-3) / 1e9
-    kernel = "build_fused_kernel" if flags == 0 else "grid_build chain (stable)"
+    kernel, sources = BUILD_KERNEL if flags == 0 else STABLE_KERNEL
     return {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
             "unit": "GB/s", "frac": achieved / peak, "algorithmic_bytes_per_launch": total_alg,
-            "traffic": kernel_traffic("build_fused.cu") if flags == 0 else None,
-            "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
+            "traffic": kernel_traffic(sources), "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
 
 
 def workload_config(scene, args) -> dict:
@@ -459,7 +467,7 @@ def run_gpu(args) -> None:
         "gather_roofline": {"kernel": "reorder_kernel (grid_reorder alone, L2 flushed before it)",
                             "achieved": gather_gbs, "peak": peak, "unit": "GB/s", "frac": gather_gbs / peak,
                             "algorithmic_bytes_per_launch": alg["gather"],
-                            "traffic": kernel_traffic("reorder.cu")},
+                            "traffic": kernel_traffic(["reorder.cu"])},
         "build_hbm": {"algorithmic_bytes": total_alg, "us_per_build": ms_per_step * 1e3,
                       "us_min": 1e3 * min(step_ms), "us_median": 1e3 * statistics.median(step_ms),
                       "achieved_gbs": gbs(ms_per_step * 1e3),
