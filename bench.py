@@ -263,9 +263,11 @@ def workload_config(scene, args) -> dict:
     return {
         "workload": (f"{scene.name}: N={scene.n:,} particles, grid {scene.dims[0]}x{scene.dims[1]}x{scene.dims[2]}"
                      f" over [-5,5)^3, 32-byte Particula AoS, {scene.kind} positions"),
-        "build": "stable" if args.stable else "atomic cursor",
+        "build": ("stable (ordenado ordered by particle index inside each cell)" if args.stable
+                  else "atomic (order inside a cell unspecified)"),
         "l2": "flushed between steps (a 2x L2 buffer is written outside the timed events)",
-        "launch": "grid_build on a stream (C ABI): one cooperative launch of the fused build kernel",
+        "launch": ("grid_build on a stream (C ABI): one cooperative launch of "
+                   + (STABLE_KERNEL[0] if args.stable else BUILD_KERNEL[0])),
     }
 
 
