@@ -64,6 +64,8 @@ static_assert(kBucketMaxCells == kScanVecs * 4 * kThreads && kBucketMaxCount == 
               "bucket tables are the 32 KB scan table");
 constexpr size_t kTableBytes = (size_t)kScanVecs * kThreads * sizeof(uint4);  // 32 KB
 constexpr size_t kDynamicSmem = kTableBytes + 3 * kBucketCap * sizeof(uint32_t);  // + 3 x 16 KB buffers
+constexpr uint32_t kCacheMax = 6144;  // particles per CTA whose cell and rank phase A keeps for phase C
+static_assert(2 * kCacheMax <= 3 * kBucketCap, "phase A's cache fits the three buffers");
 constexpr int kMaxDevices = 64;
 
 struct BucketScratch {
@@ -155,6 +157,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     uint32_t *s_order = reinterpret_cast<uint32_t *>(s_dyn + kScanVecs * kThreads);  // u32[kBucketCap]
     uint32_t *s_who = s_order + kBucketCap;                                           // u32[kBucketCap]
     uint32_t *s_place = s_who + kBucketCap;                                           // u32[kBucketCap]
+    uint32_t *s_cell = s_order, *s_rank = s_order + kCacheMax;  // phase A's cache, over the three buffers
     __shared__ uint32_t s_red[kWarps];
     __shared__ uint32_t s_rows[kScanVecs][kWarps];
     __shared__ uint32_t s_clean, s_bclean, s_base, s_count;
@@ -170,6 +173,8 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     __syncthreads();
     uint64_t p_lo, p_hi;
     particle_range(a.n, p_lo, p_hi);
+    const uint32_t mine = (uint32_t)(p_hi - p_lo);
+    const bool cached = mine <= kCacheMax;
 
     UGRID_PHASE_MARK(0);
     if (!s_bclean) {
@@ -193,13 +198,17 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
             for (int k = 0; k < kCountItems; ++k) {
                 const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
                 const bool valid = i < p_hi;
-                uint32_t bucket = 0u;
+                uint32_t bucket = 0u, c = 0u;
                 if (valid) {
-                    const uint32_t c = cell_of(rec[k], g);
+                    c = cell_of(rec[k], g);
                     a.celdaDe[i] = c;
                     bucket = bucket_of(c, bk);
                 }
-                smem_take(s_table, valid, bucket);
+                const uint32_t rank = smem_take(s_table, valid, bucket);
+                if (valid && cached) {
+                    s_cell[i - p_lo] = c;
+                    s_rank[i - p_lo] = rank;
+                }
             }
         }
     }
@@ -219,7 +228,6 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     bool heavy;
     {
         const uint32_t lane_r = blockIdx.x % kBucketLanes;
-        uint32_t *s_start = s_order;  // u32[kBucketMaxCount]: s_order and s_who are free until phase D
         uint4 v[kScanVecs];
         uint32_t t[kScanVecs], most = 0;
 #pragma unroll
@@ -232,7 +240,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
                 if (b0 + e < B) {
                     uint32_t before;
                     w[e] = bucket_total(bk.total, b0 + e, lane_r, before);
-                    s_start[b0 + e] = before;
+                    s_table[b0 + e] += before;  // this thread's own bucket: no other thread touches it
                 }
             }
             v[q] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -258,7 +266,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
                 for (int e = 0; e < 4; ++e) {
                     if (b0 + e < B) {
                         if (blockIdx.x == 0) bk.base[b0 + e] = start[e];
-                        s_table[b0 + e] += s_start[b0 + e] + start[e];  // cursor of this CTA's stretch
+                        s_table[b0 + e] += start[e];  // cursor of this CTA's stretch
                     }
                 }
                 row_base += rows[q];
@@ -271,7 +279,18 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     if (heavy) {
         atomic_path(a, g, hdr, ws, bk, s_clean != 0u, passed, p_lo, p_hi, s_held, s_red, s_rows);
     } else {
-        for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
+        if (cached) {
+            // Phase A kept each particle's cell and its rank among this CTA's
+            // particles of its bucket: the pair's place needs no atomic.
+            for (uint32_t k = tid; k < mine; k += kThreads) {
+                const uint32_t c = s_cell[k];
+                const uint32_t q = s_table[bucket_of(c, bk)] + s_rank[k];
+                if (q < a.n)
+                    bk.pairs[q] = make_uint2(c, (uint32_t)(p_lo + k));
+                else
+                    record_status(&hdr->status, kStatusBounds);
+            }
+        } else for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
             uint32_t cell[kScatterItems];
 #pragma unroll
             for (int k = 0; k < kScatterItems; ++k) {
