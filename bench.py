@@ -243,6 +243,30 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# fp32 lanes of the GPU (152 SMs x 128) and its maximum SM clock, for the
+# neighbour query's arithmetic ceiling; operations in one distance test.
+ALU_LANES = 152 * 128
+ALU_CLOCK_GHZ = 2.07
+PAIR_TEST_OPS = 7
+
+
+def pair_tests(conteos, dims) -> int:
+    """Distance tests of one neighbour query: for every particle, the
+    particles of the (up to) 27 cells around its cell, itself included.
+    conteos is in linear order (x fastest)."""
+    import numpy as np
+
+    gx, gy, gz = (int(d) for d in dims)
+    c = conteos.astype(np.int64).reshape(gz, gy, gx)
+    pad = np.pad(c, 1)
+    around = np.zeros_like(c)
+    for dz in range(3):
+        for dy in range(3):
+            for dx in range(3):
+                around += pad[dz:dz + gz, dy:dy + gy, dx:dx + gx]
+    return int((c * around).sum())
+
+
 # The kernel one non-stable grid_build launches (and the sources its DRAM
 # traffic is keyed by), and the one a stable build launches.
 BUILD_KERNEL = ("build_bucketed_kernel", ["build_bucketed.cu", "fused_common.cuh"])
@@ -444,12 +468,25 @@ def run_gpu(args) -> None:
                 raise RuntimeError(f"device status {ug.grid_status(bs.ws)} after the neighbour query")
             neighbour[f"us_{order_name}_sorted"] = 1e3 * sorted_ms
             neighbour[f"us_{order_name}_indirect"] = 1e3 * indirect_ms
+            if order == ug.GRID_ORDER_LINEAR:
+                tests = pair_tests(bs.conteos.cpu().numpy().view(np.uint32), sph.dims)
             del bs
         neighbour["reorder_gain"] = neighbour["us_linear_indirect"] / neighbour["us_linear_sorted"]
         neighbour["morton_gain_sorted"] = neighbour["us_linear_sorted"] / neighbour["us_morton_sorted"]
         neighbour["morton_gain_indirect"] = neighbour["us_linear_indirect"] / neighbour["us_morton_indirect"]
         best = min(neighbour[f"us_{o}_sorted"] for o in ("linear", "morton"))
         neighbour["mparticles_per_s_best"] = sph.n / best
+        # The query does one distance test per (particle, candidate in its 27
+        # cells): 7 fp32 operations (3 differences, 1 product, 2 fused
+        # multiply-adds, 1 comparison).  Its ceiling is the fp32 lanes at the
+        # maximum SM clock: 152 SMs x 128 lanes x 2.07 GHz / 7.
+        achieved = tests / (neighbour["us_linear_sorted"] * 1e-6) / 1e9
+        peak = ALU_LANES * ALU_CLOCK_GHZ / PAIR_TEST_OPS
+        neighbour["roofline"] = {"bound": "alu", "kernel": "density_kernel<0, 0> (linear, reordered records)",
+                                 "achieved": achieved, "peak": peak, "unit": "Gpair-tests/s",
+                                 "frac": achieved / peak, "pair_tests_per_query": int(tests),
+                                 "peak_derivation": f"{ALU_LANES} fp32 lanes x {ALU_CLOCK_GHZ} GHz / "
+                                                    f"{PAIR_TEST_OPS} ops per test"}
         del origen_s, rho
 
     if rank != 0:
