@@ -414,6 +414,42 @@ def run_gpu(args) -> None:
     peak, peak_kind = hbm_peak()
     gather_gbs = alg["gather"] / (phase_us["gather"] * 1e-6) / 1e9
 
+    # ---- the overflow diagnostics (f3) and the two-array gather (f4), cold ----
+    diag = torch.zeros(2, dtype=torch.int32, device="cuda")
+    hot = origen[:, :4].contiguous()    # pos, vida: the per-step state
+    cold = origen[:, 4:].contiguous()   # vel, masa
+    hot_out, cold_out = torch.empty_like(hot), torch.empty_like(cold)
+    next_calls = {
+        "diagnostics": lambda: ug.grid_diagnostics(b.conteos, diag, p, 64, stream),
+        "reorder_many": lambda: ug.grid_reorder_many(b.ordenado, [(hot, hot_out), (cold, cold_out)], b.ws, p, stream),
+    }
+    next_ms = {k: [] for k in next_calls}
+    for k in range(args.warmup + args.phase_steps):
+        evs = []
+        for name, call in next_calls.items():
+            settle(k)
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            e.record(stream)
+            evs.append((name, a, e))
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            for name, a, e in evs:
+                next_ms[name].append(a.elapsed_time(e))
+    check_status("the diagnostics and the two-array gather")
+    next_rows = {}
+    for name, bytes_moved, what in (
+            ("diagnostics", 4 * cells, "conteos read once (4 B per cell)"),
+            ("reorder_many", 4 * n + 2 * 32 * n, "ordenado once, a 16-B hot and a 16-B cold record read and written")):
+        us = 1e3 * statistics.mean(next_ms[name])
+        achieved = bytes_moved / (us * 1e-6) / 1e9
+        next_rows[name] = {"us": us, "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak,
+                                                  "unit": "GB/s", "frac": achieved / peak,
+                                                  "algorithmic_bytes_per_launch": bytes_moved, "bytes": what}}
+    next_rows["diagnostics"]["maxPorCelda_desbordes_at_64"] = [int(v) for v in diag.cpu().tolist()]
+    del hot, cold, hot_out, cold_out
+
     # ---- end to end: host buffers, copies inside the events ----
     host_in = torch.from_numpy(rows).pin_memory()
     host_dest = torch.empty((n, 8), dtype=torch.float32).pin_memory()
@@ -517,6 +553,7 @@ def run_gpu(args) -> None:
                   "value": n / (statistics.mean(graph_ms) / 1e3) / 1e6,
                   "frac_of_nominal_8tbs": gbs(1e3 * statistics.mean(graph_ms)) / NOMINAL_HBM_GBS},
         "phases_us_cold": phase_us,
+        "next_rows_cold": next_rows,
         "phases_gbs_cold": {k: alg[k] / (phase_us[k] * 1e-6) / 1e9 for k in phase_names},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(host_in.numel() * 4),

@@ -234,20 +234,23 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     grid_ws_header *h = header(ws);
     char *base = static_cast<char *>(ws);
-    if ((flags & GRID_STABLE) == 0 && n != 0) {
+    const bool stable = (flags & GRID_STABLE) != 0;
+    if (n != 0) {
         // The two-level counting sort in one cooperative launch (build_bucketed.cu).
         const cudaError_t f = launch_build_bucketed(
             origen, destino, conteos, celdaDe, inicios, ordenado, p->conteo, c, g, h,
             reinterpret_cast<uint32_t *>(base + l.chunk_sums), reinterpret_cast<uint32_t *>(base + l.slots),
             reinterpret_cast<uint32_t *>(base + l.counts), reinterpret_cast<uint32_t *>(base + l.bucket_total),
             reinterpret_cast<uint32_t *>(base + l.bucket_base),
-            reinterpret_cast<uint32_t *>(base + l.pairs), st);
+            reinterpret_cast<uint32_t *>(base + l.pairs), stable,
+            stable ? reinterpret_cast<uint32_t *>(base + l.stable_queue) : nullptr,
+            stable ? (uint32_t)segment_queue_capacity(n, c) : 0u,
+            stable ? reinterpret_cast<uint32_t *>(base + l.stable_scratch) : nullptr, st);
         if (f != cudaErrorNotSupported) return cuda_code(f);
         (void)cudaGetLastError();
     }
     {
         // The whole chain in one cooperative launch (build_fused.cu).
-        const bool stable = (flags & GRID_STABLE) != 0;
         const cudaError_t f = launch_build_fused(
             origen, destino, conteos, celdaDe, inicios, ordenado, p->conteo, c, g, h,
             reinterpret_cast<uint32_t *>(base + l.chunk_sums),

@@ -67,6 +67,9 @@ constexpr size_t kDynamicSmem = kTableBytes + 3 * kBucketCap * sizeof(uint32_t);
 constexpr uint32_t kCacheMax = 6144;  // particles per CTA whose cell and rank phase A keeps for phase C
 static_assert(2 * kCacheMax <= 3 * kBucketCap, "phase A's cache fits the three buffers");
 constexpr int kMaxDevices = 64;
+// Stable mode: cells of one bucket longer than kRegisterMax particles; at most
+// kBucketCap / (kRegisterMax + 1) of them fit in a bucket.
+constexpr uint32_t kLongMax = kBucketCap / (kRegisterMax + 1) + 1;
 
 struct BucketScratch {
     uint32_t width;              // cells per bucket
@@ -123,8 +126,9 @@ __device__ __forceinline__ uint32_t smem_take(uint32_t *table, bool valid, uint3
 }
 
 // A bucket too large for one CTA: every CTA takes the atomic path of the
-// fused build from celdaDe on.  Kept out of line so that its registers do not
-// weigh on the bucketed phases.
+// fused build from celdaDe on (with its stable tail in stable mode).  Kept out
+// of line so that its registers do not weigh on the bucketed phases.
+template <bool kStable>
 __device__ __noinline__ void atomic_path(const BuildArgs a, const Geometry g, grid_ws_header *hdr,
                                          const FusedScratch ws, const BucketScratch bk, bool clean,
                                          uint32_t &passed, uint64_t p_lo, uint64_t p_hi, uint4 (*s_held)[kThreads],
@@ -146,9 +150,13 @@ __device__ __noinline__ void atomic_path(const BuildArgs a, const Geometry g, gr
     grid_barrier(hdr, passed);
     if (blockIdx.x == 0 && threadIdx.x == 0 && (hdr->status & kStatusTimeout) == 0)
         hdr->counts_clean = (uint32_t)a.cells;
-    scatter_move_phase(a, ws, &hdr->status, p_lo, p_hi);
+    if constexpr (kStable)
+        stable_tail_phase(a, ws, hdr, passed, p_lo, p_hi, s_held);
+    else
+        scatter_move_phase(a, ws, &hdr->status, p_lo, p_hi);
 }
 
+template <bool kStable>
 __global__ void __launch_bounds__(kThreads, 2)
 build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch ws, BucketScratch bk) {
     extern __shared__ uint4 s_dyn[];
@@ -160,7 +168,8 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     uint32_t *s_cell = s_order, *s_rank = s_order + kCacheMax;  // phase A's cache, over the three buffers
     __shared__ uint32_t s_red[kWarps];
     __shared__ uint32_t s_rows[kScanVecs][kWarps];
-    __shared__ uint32_t s_clean, s_bclean, s_base, s_count;
+    __shared__ uint32_t s_clean, s_bclean, s_base, s_count, s_nlong;
+    __shared__ uint32_t s_long[kLongMax];  // stable mode: cells of the bucket with more than 32 particles
     const uint32_t tid = threadIdx.x;
     const uint32_t ctas = gridDim.x;
     const uint32_t B = bk.buckets;
@@ -170,6 +179,8 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
         s_bclean = *reinterpret_cast<volatile uint32_t *>(&hdr->buckets_clean) != 0u;
     }
     for (uint32_t b = tid; b < kBucketMaxCount; b += kThreads) s_table[b] = 0u;
+    // Nobody touches the long-segment queue of the atomic path before its stable tail.
+    if (kStable && blockIdx.x == 0 && tid == 0) hdr->stable_big = 0u;
     __syncthreads();
     uint64_t p_lo, p_hi;
     particle_range(a.n, p_lo, p_hi);
@@ -277,7 +288,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
 
     UGRID_PHASE_MARK(2);
     if (heavy) {
-        atomic_path(a, g, hdr, ws, bk, s_clean != 0u, passed, p_lo, p_hi, s_held, s_red, s_rows);
+        atomic_path<kStable>(a, g, hdr, ws, bk, s_clean != 0u, passed, p_lo, p_hi, s_held, s_red, s_rows);
     } else {
         if (cached) {
             // Phase A kept each particle's cell and its rank among this CTA's
@@ -319,6 +330,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
             const uint64_t cl = (uint64_t)b * bk.width;
             const uint32_t w = (uint32_t)min((uint64_t)bk.width, a.cells - cl);
             if (tid == 0) {
+                s_nlong = 0u;
                 s_base = bk.base[b];
                 uint32_t unused;
                 s_count = bucket_total(bk.total, b, 0u, unused);
@@ -387,6 +399,32 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
                 }
             }
             __syncthreads();
+            if constexpr (kStable) {
+                // Every cell's segment of the bucket sorted by particle index
+                // ("Construir el índice…", §El orden dentro de la celda):
+                // short ones by one thread in registers, the rest by the whole
+                // CTA, one at a time, in shared memory.
+                for (uint32_t l = tid; l < w; l += kThreads) {
+                    const uint32_t s0 = s_table[l] - base, e0 = (l + 1 < w ? s_table[l + 1] : base + t) - base;
+                    if (e0 > s0 + 1 && e0 <= t && !sort_short_segment(s_order + s0, e0 - s0)) {
+                        const uint32_t q = atomicAdd(&s_nlong, 1u);
+                        if (q < kLongMax)
+                            s_long[q] = l;
+                        else
+                            record_status(&hdr->status, kStatusBounds);
+                    }
+                }
+                __syncthreads();
+                const uint32_t nlong = min(s_nlong, kLongMax);
+                for (uint32_t q = 0; q < nlong; ++q) {
+                    const uint32_t l = s_long[q];
+                    const uint32_t s0 = s_table[l] - base, e0 = (l + 1 < w ? s_table[l + 1] : base + t) - base;
+                    for (uint32_t i = tid; i < e0 - s0; i += kThreads) s_who[i] = s_order[s0 + i];
+                    bitonic_shared<kThreads>(s_who, e0 - s0);
+                    for (uint32_t i = tid; i < e0 - s0; i += kThreads) s_order[s0 + i] = s_who[i];
+                    __syncthreads();
+                }
+            }
             UGRID_PHASE_MARK(7);
             for (uint32_t q = tid; q < t; q += kThreads) a.ordenado[base + q] = s_order[q];
             // The bucket's records, gathered in order ("El kernel de
@@ -421,27 +459,29 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     }
 }
 
-std::atomic<int> g_grid[kMaxDevices];  // cached grid size per device (0 = not yet known)
+std::atomic<int> g_grid[2][kMaxDevices];  // cached grid size per mode and device (0 = not yet known)
 
+template <bool kStable>
 cudaError_t bucketed_grid(int device, int *grid) {
     if (device >= 0 && device < kMaxDevices) {
-        const int cached = g_grid[device].load(std::memory_order_relaxed);
+        const int cached = g_grid[kStable][device].load(std::memory_order_relaxed);
         if (cached != 0) {
             *grid = cached;
             return cached > 0 ? cudaSuccess : cudaErrorNotSupported;
         }
     }
     int coop = 0, sms = 0, per_sm = 0;
-    cudaError_t e = cudaFuncSetAttribute(build_bucketed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(build_bucketed_kernel<kStable>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kDynamicSmem);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_bucketed_kernel, kThreads, kDynamicSmem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_bucketed_kernel<kStable>, kThreads,
+                                                          kDynamicSmem);
     if (e != cudaSuccess) return e;
     int gsz = coop ? per_sm * sms : -1;
     if (gsz <= 0 || gsz > (int)kFusedMaxCtas) gsz = -1;
-    if (device >= 0 && device < kMaxDevices) g_grid[device].store(gsz, std::memory_order_relaxed);
+    if (device >= 0 && device < kMaxDevices) g_grid[kStable][device].store(gsz, std::memory_order_relaxed);
     *grid = gsz;
     return gsz > 0 ? cudaSuccess : cudaErrorNotSupported;
 }
@@ -452,10 +492,11 @@ cudaError_t launch_build_bucketed(const ugrid_particula *origen, ugrid_particula
                                   uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, uint32_t n,
                                   uint64_t cells, const Geometry &g, grid_ws_header *hdr, uint32_t *chunk_sums,
                                   uint32_t *slots, uint32_t *counts, uint32_t *total, uint32_t *base,
-                                  uint32_t *pairs, cudaStream_t s) {
+                                  uint32_t *pairs, bool stable, uint32_t *queue, uint32_t queue_capacity,
+                                  uint32_t *sort_scratch, cudaStream_t s) {
     int device = 0, grid = 0;
     cudaError_t e = cudaGetDevice(&device);
-    if (e == cudaSuccess) e = bucketed_grid(device, &grid);
+    if (e == cudaSuccess) e = stable ? bucketed_grid<true>(device, &grid) : bucketed_grid<false>(device, &grid);
     if (e != cudaSuccess) return e;
     const BucketPlan plan = bucket_plan(n, cells, (uint32_t)grid);
     if (plan.buckets == 0) return cudaErrorNotSupported;
@@ -469,11 +510,12 @@ cudaError_t launch_build_bucketed(const ugrid_particula *origen, ugrid_particula
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const FusedScratch ws{chunk_sums, slots, counts, nullptr, 0u, nullptr};
+    const FusedScratch ws{chunk_sums, slots, counts, queue, queue_capacity, sort_scratch};
     const BucketScratch bk{plan.width, plan.buckets, plan.magic, total, base, reinterpret_cast<uint2 *>(pairs)};
     const BuildArgs a{reinterpret_cast<const uint4 *>(origen), reinterpret_cast<uint4 *>(destino), conteos, celdaDe,
                       inicios, ordenado, n, cells};
-    return cudaLaunchKernelEx(&cfg, build_bucketed_kernel, a, g, hdr, ws, bk);
+    return cudaLaunchKernelEx(&cfg, stable ? build_bucketed_kernel<true> : build_bucketed_kernel<false>, a, g, hdr,
+                              ws, bk);
 }
 
 }  // namespace ugrid

@@ -117,94 +117,7 @@ build_fused_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch ws
     if constexpr (!kStable) {
         scatter_move_phase(a, ws, &hdr->status, p_lo, p_hi);
     } else {
-        // ---- stable mode: scatter the indices, sort each cell, then gather ---
-        for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
-            uint32_t cell[kScatterItems], slot[kScatterItems], start[kScatterItems];
-#pragma unroll
-            for (int k = 0; k < kScatterItems; ++k) {
-                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-                if (i < p_hi) {
-                    cell[k] = a.celdaDe[i];
-                    slot[k] = ws.slots[i];
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < kScatterItems; ++k) {
-                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-                if (i < p_hi) start[k] = a.inicios[cell[k]];
-            }
-#pragma unroll
-            for (int k = 0; k < kScatterItems; ++k) {
-                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-                if (i < p_hi) {
-                    const uint32_t pos = start[k] + slot[k];
-                    if (pos < a.n)
-                        a.ordenado[pos] = (uint32_t)i;
-                    else
-                        record_status(&hdr->status, kStatusBounds);
-                }
-            }
-        }
-        UGRID_PHASE_END(4);
-        grid_barrier(hdr, passed);
-
-        // Every cell's segment sorted by particle index ("Construir el
-        // índice…", §El orden dentro de la celda).  Short segments are sorted
-        // by one thread in registers; longer ones are queued.
-        const uint64_t grid_threads = (uint64_t)ctas * kThreads;
-        for (uint64_t c = (uint64_t)blockIdx.x * kThreads + tid; c < a.cells; c += grid_threads) {
-            const uint32_t s = a.inicios[c];
-            if (!sort_short_segment(a.ordenado + s, a.inicios[c + 1] - s)) {
-                const uint32_t q = atomicAdd(&hdr->stable_big, 1u);
-                if (q < ws.queue_capacity)
-                    ws.queue[q] = (uint32_t)c;
-                else
-                    record_status(&hdr->status, kStatusBounds);
-            }
-        }
-        grid_barrier(hdr, passed);
-        // Long segments, one CTA each: bitonic in shared memory up to 8192
-        // indices, radix through the workspace scratch beyond.
-        const uint32_t queued = *reinterpret_cast<volatile uint32_t *>(&hdr->stable_big);
-        const uint32_t count = min(queued, ws.queue_capacity);
-        uint32_t *s_buf = reinterpret_cast<uint32_t *>(&s_held[0][0]);
-        for (uint32_t q = blockIdx.x; q < count; q += ctas) {
-            const uint32_t c = ws.queue[q];
-            const uint32_t s = a.inicios[c];
-            sort_long_segment<kThreads>(a.ordenado + s, ws.sort_scratch + s, a.inicios[c + 1] - s, a.n, s_buf,
-                                        kScanVecs * kThreads * 4);
-        }
-        grid_barrier(hdr, passed);
-
-        UGRID_PHASE_MARK(5);
-        // Gather, two threads per 32-byte record.
-        unsigned long long last_use;
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(last_use));
-        const uint64_t h_lo = 2 * p_lo, h_hi = 2 * p_hi;
-        for (uint64_t r0 = h_lo; r0 < h_hi; r0 += (uint64_t)kThreads * kGatherItems) {
-            uint32_t src[kGatherItems];
-#pragma unroll
-            for (int k = 0; k < kGatherItems; ++k) {
-                const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
-                src[k] = h < h_hi ? a.ordenado[h >> 1] : 0u;
-            }
-            uint4 v[kGatherItems];
-#pragma unroll
-            for (int k = 0; k < kGatherItems; ++k) {
-                const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
-                if (h < h_hi && src[k] < a.n) v[k] = load_policy(a.origen + 2 * (uint64_t)src[k] + (h & 1), last_use);
-            }
-#pragma unroll
-            for (int k = 0; k < kGatherItems; ++k) {
-                const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
-                if (h < h_hi) {
-                    if (src[k] < a.n)
-                        store_cs(a.destino + h, v[k]);
-                    else if ((h & 1) == 0)
-                        record_status(&hdr->status, kStatusBounds);
-                }
-            }
-        }
+        stable_tail_phase(a, ws, hdr, passed, p_lo, p_hi, s_held);
     }
     UGRID_PHASE_MARK(6);
     leave_launch(hdr);

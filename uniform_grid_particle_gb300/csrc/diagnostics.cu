@@ -15,16 +15,19 @@
 namespace ugrid {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 
 __global__ void __launch_bounds__(kThreads)
 diagnostics_kernel(const uint32_t *__restrict__ conteos, uint64_t cells, uint32_t capacidad,
                    uint32_t *diag) {
+    __shared__ uint32_t s_most[kWarps], s_over[kWarps];
     const uint64_t stride = (uint64_t)gridDim.x * kThreads;
     const uint64_t first = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
     uint32_t most = 0, over = 0;
     const uint64_t quads = cells / 4;
     const uint4 *c4 = reinterpret_cast<const uint4 *>(conteos);
+#pragma unroll 4
     for (uint64_t q = first; q < quads; q += stride) {
         const uint4 v = c4[q];
         most = max(max(most, max(v.x, v.y)), max(v.z, v.w));
@@ -36,11 +39,24 @@ diagnostics_kernel(const uint32_t *__restrict__ conteos, uint64_t cells, uint32_
         most = max(most, v);
         over += v > capacidad ? v - capacidad : 0u;
     }
+    // Warp, then block: one pair of atomics per block, so the two words are
+    // not a queue of thousands of same-address atomics.
     most = __reduce_max_sync(0xffffffffu, most);
     over = __reduce_add_sync(0xffffffffu, over);
     if (lane_id() == 0) {
-        if (most) atomicMax(diag, most);
-        if (over) atomicAdd(diag + 1, over);
+        s_most[threadIdx.x >> 5] = most;
+        s_over[threadIdx.x >> 5] = over;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        most = threadIdx.x < kWarps ? s_most[threadIdx.x] : 0u;
+        over = threadIdx.x < kWarps ? s_over[threadIdx.x] : 0u;
+        most = __reduce_max_sync(0xffffffffu, most);
+        over = __reduce_add_sync(0xffffffffu, over);
+        if (threadIdx.x == 0) {
+            if (most) atomicMax(diag, most);
+            if (over) atomicAdd(diag + 1, over);
+        }
     }
 }
 
@@ -54,8 +70,9 @@ cudaError_t launch_diagnostics(const uint32_t *conteos, uint64_t cells, uint32_t
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
         return e;
+    // Two blocks per SM at most: every thread has a few 16-byte loads in flight.
     const uint64_t want = (cells / 4 + kThreads - 1) / kThreads;
-    const unsigned blocks = (unsigned)(want < 1 ? 1 : (want < (uint64_t)sms * 8 ? want : (uint64_t)sms * 8));
+    const unsigned blocks = (unsigned)(want < 1 ? 1 : (want < (uint64_t)sms * 2 ? want : (uint64_t)sms * 2));
     return launch(diagnostics_kernel, blocks, kThreads, 0, s, false, conteos, cells, capacidad, diag);
 }
 

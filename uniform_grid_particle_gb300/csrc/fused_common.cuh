@@ -432,6 +432,105 @@ __device__ __forceinline__ void scatter_move_phase(const BuildArgs &a, const Fus
     }
 }
 
+// ---- stable tail: scatter the indices, sort each cell, then gather -------------
+// ("Construir el índice…", §El orden dentro de la celda: particle index as the
+// tie-break.)  The scatter places particle i at inicios[c] + slots[i]; one
+// thread per cell sorts its segment in registers when it holds at most 32
+// particles and queues it otherwise; CTAs then take the queued segments one
+// each (bitonic in shared memory up to 8192, an LSD radix sort through the
+// workspace beyond); finally the records are gathered in the sorted order.
+__device__ __forceinline__ void stable_tail_phase(const BuildArgs &a, const FusedScratch &ws, grid_ws_header *hdr,
+                                                  uint32_t &passed, uint64_t p_lo, uint64_t p_hi,
+                                                  uint4 (*s_held)[kThreads]) {
+    const uint32_t tid = threadIdx.x;
+    const uint32_t ctas = gridDim.x;
+    for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
+        uint32_t cell[kScatterItems], slot[kScatterItems], start[kScatterItems];
+#pragma unroll
+        for (int k = 0; k < kScatterItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+            if (i < p_hi) {
+                cell[k] = a.celdaDe[i];
+                slot[k] = ws.slots[i];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kScatterItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+            if (i < p_hi) start[k] = a.inicios[cell[k]];
+        }
+#pragma unroll
+        for (int k = 0; k < kScatterItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
+            if (i < p_hi) {
+                const uint32_t pos = start[k] + slot[k];
+                if (pos < a.n)
+                    a.ordenado[pos] = (uint32_t)i;
+                else
+                    record_status(&hdr->status, kStatusBounds);
+            }
+        }
+    }
+    grid_barrier(hdr, passed);
+
+    // Every cell's segment sorted by particle index ("Construir el
+    // índice…", §El orden dentro de la celda).  Short segments are sorted
+    // by one thread in registers; longer ones are queued.
+    const uint64_t grid_threads = (uint64_t)ctas * kThreads;
+    for (uint64_t c = (uint64_t)blockIdx.x * kThreads + tid; c < a.cells; c += grid_threads) {
+        const uint32_t s = a.inicios[c];
+        if (!sort_short_segment(a.ordenado + s, a.inicios[c + 1] - s)) {
+            const uint32_t q = atomicAdd(&hdr->stable_big, 1u);
+            if (q < ws.queue_capacity)
+                ws.queue[q] = (uint32_t)c;
+            else
+                record_status(&hdr->status, kStatusBounds);
+        }
+    }
+    grid_barrier(hdr, passed);
+    // Long segments, one CTA each: bitonic in shared memory up to 8192
+    // indices, radix through the workspace scratch beyond.
+    const uint32_t queued = *reinterpret_cast<volatile uint32_t *>(&hdr->stable_big);
+    const uint32_t count = min(queued, ws.queue_capacity);
+    uint32_t *s_buf = reinterpret_cast<uint32_t *>(&s_held[0][0]);
+    for (uint32_t q = blockIdx.x; q < count; q += ctas) {
+        const uint32_t c = ws.queue[q];
+        const uint32_t s = a.inicios[c];
+        sort_long_segment<kThreads>(a.ordenado + s, ws.sort_scratch + s, a.inicios[c + 1] - s, a.n, s_buf,
+                                    kScanVecs * kThreads * 4);
+    }
+    grid_barrier(hdr, passed);
+
+    // Gather, two threads per 32-byte record.
+    unsigned long long last_use;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(last_use));
+    const uint64_t h_lo = 2 * p_lo, h_hi = 2 * p_hi;
+    for (uint64_t r0 = h_lo; r0 < h_hi; r0 += (uint64_t)kThreads * kGatherItems) {
+        uint32_t src[kGatherItems];
+#pragma unroll
+        for (int k = 0; k < kGatherItems; ++k) {
+            const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+            src[k] = h < h_hi ? a.ordenado[h >> 1] : 0u;
+        }
+        uint4 v[kGatherItems];
+#pragma unroll
+        for (int k = 0; k < kGatherItems; ++k) {
+            const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+            if (h < h_hi && src[k] < a.n) v[k] = load_policy(a.origen + 2 * (uint64_t)src[k] + (h & 1), last_use);
+        }
+#pragma unroll
+        for (int k = 0; k < kGatherItems; ++k) {
+            const uint64_t h = r0 + (uint64_t)k * kThreads + tid;
+            if (h < h_hi) {
+                if (src[k] < a.n)
+                    store_cs(a.destino + h, v[k]);
+                else if ((h & 1) == 0)
+                    record_status(&hdr->status, kStatusBounds);
+            }
+        }
+    }
+}
+
 // The last CTA out of a launch resets the barrier counter for the next one.
 __device__ __forceinline__ void leave_launch(grid_ws_header *hdr) {
     if (threadIdx.x == 0 && atomicAdd(&hdr->bar_exit, 1u) == gridDim.x - 1u) {

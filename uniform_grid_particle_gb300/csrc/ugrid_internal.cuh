@@ -142,7 +142,8 @@ cudaError_t launch_build_bucketed(const ugrid_particula *origen, ugrid_particula
                                   uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, uint32_t n,
                                   uint64_t cells, const Geometry &g, grid_ws_header *hdr, uint32_t *chunk_sums,
                                   uint32_t *slots, uint32_t *counts, uint32_t *total, uint32_t *base,
-                                  uint32_t *pairs, cudaStream_t s);
+                                  uint32_t *pairs, bool stable, uint32_t *queue, uint32_t queue_capacity,
+                                  uint32_t *sort_scratch, cudaStream_t s);
 
 // Several arrays gathered with one ordenado (grid_reorder_many).
 constexpr int kMaxArrays = 4;
