@@ -517,11 +517,11 @@ def run_gpu(args) -> None:
         # cells): 7 fp32 operations (3 differences, 1 product, 2 fused
         # multiply-adds, 1 comparison).  Its ceiling is the fp32 lanes at the
         # maximum SM clock: 152 SMs x 128 lanes x 2.07 GHz / 7.
-        achieved = tests / (neighbour["us_linear_sorted"] * 1e-6) / 1e9
-        peak = ALU_LANES * ALU_CLOCK_GHZ / PAIR_TEST_OPS
+        tests_per_s = tests / (neighbour["us_linear_sorted"] * 1e-6) / 1e9
+        alu_peak = ALU_LANES * ALU_CLOCK_GHZ / PAIR_TEST_OPS
         neighbour["roofline"] = {"bound": "alu", "kernel": "density_kernel<0, 0> (linear, reordered records)",
-                                 "achieved": achieved, "peak": peak, "unit": "Gpair-tests/s",
-                                 "frac": achieved / peak, "pair_tests_per_query": int(tests),
+                                 "achieved": tests_per_s, "peak": alu_peak, "unit": "Gpair-tests/s",
+                                 "frac": tests_per_s / alu_peak, "pair_tests_per_query": int(tests),
                                  "peak_derivation": f"{ALU_LANES} fp32 lanes x {ALU_CLOCK_GHZ} GHz / "
                                                     f"{PAIR_TEST_OPS} ops per test"}
         del origen_s, rho
