@@ -113,6 +113,21 @@ def test_stable_mode_is_deterministic(ug, oracle_lib):
     assert np.array_equal(a["destino"].view(np.uint32), b["destino"].view(np.uint32))
 
 
+@pytest.mark.parametrize("crowd", [33, 200, 2000], ids=["crowd33", "crowd200", "crowd2000"])
+def test_stable_crowded_cell_inside_a_bucket(ug, oracle_lib, crowd):
+    """A cell of more than 32 particles whose bucket still fits one CTA: the
+    bucketed build sorts that segment with the CTA's shared-memory bitonic
+    sort (shorter ones in registers).  The crowd is interleaved with the rest
+    so its particle indices are scattered."""
+    rng = np.random.default_rng(crowd)
+    base = scenes.uniform_particles(100_000, 31)
+    rows = np.concatenate([base, base[:crowd].copy()])
+    rows[-crowd:, :3] = np.float32(0.01)  # all in the cell holding (0.01, 0.01, 0.01)
+    rows = rows[rng.permutation(rows.shape[0])]
+    for stable in (True, False):
+        _check(ug, oracle_lib, rows, (128,) * 3, (-5.0,) * 3, 0.078125, stable)
+
+
 # ---------------------------------------------------------------- one entry point at a time
 
 def test_phases_one_by_one(ug, oracle_lib):
