@@ -329,20 +329,22 @@ def run_gpu(args) -> None:
         ug.grid_build(origen, b.destino, b.conteos, b.celdaDe, b.inicios, b.ordenado, b.ws, p, flags,
                       torch.cuda.current_stream())
 
-    def settle(k):
-        """Untimed: flush L2, then hold the stream briefly so that the host
-        has enqueued the whole step before the GPU reaches its start event."""
-        flush.fill_(k & 0x7F)
+    def settle(k, cold=True):
+        """Untimed: flush L2 (unless warm), then hold the stream briefly so
+        that the host has enqueued the whole step before the GPU reaches its
+        start event."""
+        if cold:
+            flush.fill_(k & 0x7F)
         if sleep is not None:
             sleep(40_000)
 
-    def timed(run, steps):
+    def timed(run, steps, cold=True):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         barrier(dist)
         torch.cuda.synchronize()
         for k in range(steps):
-            settle(k)
+            settle(k, cold)
             starts[k].record(stream)
             run()
             ends[k].record(stream)
@@ -367,7 +369,7 @@ def run_gpu(args) -> None:
     total_ms = max_over_ranks(sum(step_ms), dist)
     ms_per_step = total_ms / args.steps
     value = job_rate(world, n, ms_per_step)
-    kernels_per_step = 1 if not args.stable else 6   # the fused kernel; the stable chain launches six
+    kernels_per_step = 1   # one cooperative launch of the build kernel, stable or not
 
     # ---- the same build replayed from a CUDA graph ----
     graph = torch.cuda.CUDAGraph()
@@ -384,6 +386,49 @@ def run_gpu(args) -> None:
         graph.replay()
     graph_ms = timed(graph.replay, min(args.steps, args.graph_steps))
     check_status("the graph steps")
+
+    # ---- warm L2, and an input already in cell order (context) ----
+    warm_ms = timed(step, min(args.steps, args.graph_steps), cold=False)
+    sorted_in = b.destino.clone()     # the last build's records: already in cell order
+    b_sorted = ug.GridBuffers.allocate(p, flags)
+
+    def step_sorted():
+        ug.grid_build(sorted_in, b_sorted.destino, b_sorted.conteos, b_sorted.celdaDe, b_sorted.inicios,
+                      b_sorted.ordenado, b_sorted.ws, p, flags, torch.cuda.current_stream())
+
+    for k in range(args.warmup):
+        settle(k)
+        step_sorted()
+    sorted_ms = timed(step_sorted, min(args.steps, args.graph_steps))
+    if ug.grid_status(b_sorted.ws) != 0:
+        raise RuntimeError("device status set during the sorted-input builds")
+    del sorted_in, b_sorted
+    context = {"warm_l2_us": 1e3 * statistics.mean(warm_ms),
+               "sorted_input_us": 1e3 * statistics.mean(sorted_ms),
+               "sorted_input": "the previous build's destino (particles already in cell order), L2 flushed"}
+
+    # ---- repeated builds of one scene, origen and destino swapped (stress) ----
+    if scene.builds > 1:
+        pong = ug.GridBuffers.allocate(p, flags)
+        src, bufs = origen.clone(), [b, pong]
+        seq_ms = []
+        for k in range(scene.builds):
+            dst = bufs[k % 2]
+            settle(k)
+            a_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(stream)
+            ug.grid_build(src, dst.destino, dst.conteos, dst.celdaDe, dst.inicios, dst.ordenado, dst.ws, p, flags,
+                          stream)
+            e_ev.record(stream)
+            torch.cuda.synchronize()
+            seq_ms.append(a_ev.elapsed_time(e_ev))
+            if ug.grid_status(dst.ws) != 0:
+                raise RuntimeError("device status set during the ping-pong builds")
+            src = dst.destino  # the next build reads this one's output, into the other buffers
+        context["ping_pong"] = {"builds": scene.builds, "build1_us": 1e3 * seq_ms[0],
+                                "builds_2_on_mean_us": 1e3 * statistics.mean(seq_ms[1:]),
+                                "note": "build k+1 reads build k's destino; L2 flushed before each"}
+        del pong, src
 
     # ---- phase pass: each phase alone, L2 flushed before each (cold) ----
     phase_names = ["clear", "count", "scan", "clear_cursor", "scatter", "gather"]
@@ -553,6 +598,7 @@ def run_gpu(args) -> None:
                   "us_median": 1e3 * statistics.median(graph_ms),
                   "value": n / (statistics.mean(graph_ms) / 1e3) / 1e6,
                   "frac_of_nominal_8tbs": gbs(1e3 * statistics.mean(graph_ms)) / NOMINAL_HBM_GBS},
+        "context": context,
         "phases_us_cold": phase_us,
         "next_rows_cold": next_rows,
         "phases_gbs_cold": {k: alg[k] / (phase_us[k] * 1e-6) / 1e9 for k in phase_names},
