@@ -128,6 +128,17 @@ def test_stable_crowded_cell_inside_a_bucket(ug, oracle_lib, crowd):
         _check(ug, oracle_lib, rows, (128,) * 3, (-5.0,) * 3, 0.078125, stable)
 
 
+@pytest.mark.parametrize("stable", [False, True], ids=["atomic", "stable"])
+@pytest.mark.parametrize("name", ["headline", "scan_dominated", "contention"])
+def test_input_already_in_cell_order(ug, oracle_lib, name, stable):
+    """A second build from the first build's destino: equal keys arrive in
+    runs, which takes the shared-memory counters' run-length path."""
+    s = scenes.SCENES[name]
+    first = gpu_build(ug, s.particles(), s.dims, s.origin, s.cell_size)
+    rows = np.ascontiguousarray(first["destino"])
+    _check(ug, oracle_lib, rows, s.dims, s.origin, s.cell_size, stable)
+
+
 # ---------------------------------------------------------------- one entry point at a time
 
 def test_phases_one_by_one(ug, oracle_lib):

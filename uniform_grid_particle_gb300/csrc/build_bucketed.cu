@@ -109,20 +109,35 @@ __device__ __forceinline__ void zero_bucket(uint32_t *total, uint32_t b) {
 // Shared-memory add of 1 to table[key] for every valid lane; returns the
 // value before this lane's add.  Lanes of a warp that share a key are served
 // by one atomic of their leader when the cheap adjacent-duplicate test finds
-// any, so crowded keys do not serialise.
+// any, so crowded keys do not serialise.  When the valid lanes are a prefix of
+// the warp and their keys do not decrease (input already in cell order), the
+// runs of equal keys are found with one ballot: each run's first lane adds
+// the run's length.  Otherwise __match_any_sync groups the lanes.
 __device__ __forceinline__ uint32_t smem_take(uint32_t *table, bool valid, uint32_t key) {
-    if (warp_has_adjacent_duplicates(valid, key)) {
-        const uint32_t active = __ballot_sync(0xffffffffu, valid);
-        uint32_t first = 0u, peers = 0u;
-        if (valid) {
-            peers = __match_any_sync(active, key);
-            const uint32_t leader = (uint32_t)(__ffs(peers) - 1);
-            if (lane_id() == leader) first = atomicAdd(&table[key], (uint32_t)__popc(peers));
-            first = __shfl_sync(peers, first, leader);
-        }
-        return first + (uint32_t)__popc(peers & lanemask_lt());
+    if (!warp_has_adjacent_duplicates(valid, key)) return valid ? atomicAdd(&table[key], 1u) : 0u;
+    const uint32_t lane = lane_id();
+    const uint32_t active = __ballot_sync(0xffffffffu, valid);
+    const uint32_t below = __shfl_up_sync(0xffffffffu, key, 1);
+    const bool prefix = (active & (active + 1u)) == 0u;  // lanes 0..k-1 valid, the rest not
+    if (prefix && __all_sync(0xffffffffu, !valid || lane == 0 || below <= key)) {
+        const uint32_t heads = __ballot_sync(0xffffffffu, valid && (lane == 0 || below != key));
+        const uint32_t upto = lane == 31 ? 0xffffffffu : (2u << lane) - 1u;
+        const uint32_t start = 31u - (uint32_t)__clz(heads & upto);
+        const uint32_t later = (heads | ~active) & ~upto;  // the next run's head, or the first invalid lane
+        const uint32_t end = later ? (uint32_t)(__ffs(later) - 1) : 32u;
+        uint32_t first = 0u;
+        if (valid && lane == start) first = atomicAdd(&table[key], end - start);
+        first = __shfl_sync(0xffffffffu, first, start);
+        return valid ? first + (lane - start) : 0u;
     }
-    return valid ? atomicAdd(&table[key], 1u) : 0u;
+    uint32_t first = 0u, peers = 0u;
+    if (valid) {
+        peers = __match_any_sync(active, key);
+        const uint32_t leader = (uint32_t)(__ffs(peers) - 1);
+        if (lane == leader) first = atomicAdd(&table[key], (uint32_t)__popc(peers));
+        first = __shfl_sync(peers, first, leader);
+    }
+    return first + (uint32_t)__popc(peers & lanemask_lt());
 }
 
 // A bucket too large for one CTA: every CTA takes the atomic path of the
