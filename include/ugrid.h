@@ -108,8 +108,8 @@ typedef struct grid_ws_header {
     uint32_t scan_done;    /* tiles finished by the running scan; 0 between calls */
     uint32_t stable_big;   /* cells queued for the long-segment sort; 0 between calls */
     uint32_t stable_done;  /* CTAs finished by the running long-segment sort; 0 between calls */
-    uint32_t bar_count;    /* grid-barrier arrivals of the running fused build; 0 between calls */
-    uint32_t bar_exit;     /* CTAs that finished the running fused build; 0 between calls */
+    uint32_t bar_count;    /* grid-barrier arrivals of the running single-launch build; 0 between calls */
+    uint32_t bar_exit;     /* CTAs that finished the running single-launch build; 0 between calls */
     uint32_t counts_clean; /* cells of the fused build's counter array known to be zero */
     uint32_t buckets_clean; /* 1 when the bucketed build's per-bucket totals are all zero */
     uint32_t reserved[55];
@@ -117,8 +117,9 @@ typedef struct grid_ws_header {
 
 /* Bytes of device workspace the calls below need for these params and flags
  * (the header, the scan's per-tile look-back status words, grid_build's
- * per-CTA chunk sums, per-particle slots and per-cell counter array and, with
- * GRID_STABLE, the segment-sort queue and scratch).  Returns 0 for invalid
+ * per-CTA chunk sums, per-particle slots, per-cell counter array, per-bucket
+ * totals and first positions and per-particle (cell, particle) pairs and,
+ * with GRID_STABLE, the segment-sort queue and scratch).  Returns 0 for invalid
  * params.  The workspace must be 256-byte aligned and zero-filled once after
  * allocation (grid_workspace_init does that); every call leaves it ready for
  * the next one.  A workspace sized for one params/flags is valid for any
@@ -146,7 +147,7 @@ int grid_count(const ugrid_particula *parts, uint32_t *conteos, uint32_t *celdaD
 /* a3 — exclusive scan with the total in an extra slot ("Construir el índice de
  * la rejilla…", §Del conteo al inicio):
  *   inicios[0] = 0, inicios[c+1] = inicios[c] + conteos[c], inicios[C] = N.
- * Single pass with decoupled look-back over tiles of 4096 cells.
+ * Single pass with decoupled look-back over tiles of 8192 cells.
  * conteos: u32[C] (read only).  inicios: u32[C+1] (written).  Both 16-byte
  * aligned and distinct.  ws: workspace (see grid_workspace_bytes). */
 int grid_scan(const uint32_t *conteos, uint32_t *inicios, void *ws, const grid_params *p,
@@ -174,13 +175,20 @@ int grid_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cur
 int grid_reorder(const uint32_t *ordenado, const ugrid_particula *origen, ugrid_particula *destino,
                  void *ws, const grid_params *p, void *stream);
 
-/* The whole build, in the order the pages give ("Construir el índice de la
- * rejilla…", §La cadena completa): clear conteos, count, scan, clear the
- * cursor (= conteos), scatter, [segment sort], gather.  The second clear is
- * folded into the scan, which zeroes each tile of conteos after reading it.
+/* The whole build: what the pages' chain computes ("Construir el índice de
+ * la rejilla…", §La cadena completa: clear conteos, count, scan, clear the
+ * cursor, scatter, [segment sort], gather), in one cooperative launch.  The
+ * particles are first sorted into buckets of consecutive cells with shared-
+ * memory counters, then each bucket's cells are counted, scanned and placed by
+ * one CTA (a two-level counting sort); a bucket too large for one CTA sends
+ * the launch down an atomic-counter path, and grids of more than 8192 buckets
+ * use that path from the start.  Where a cooperative launch is not available
+ * the entry points above run one after the other, the second clear folded
+ * into the scan.
  * On return (once the stream has run) conteos holds the histogram, celdaDe the
  * cells, inicios the starts, ordenado the cell-grouped indices and destino
- * the reordered records.  All seven arrays must be distinct. */
+ * the reordered records; without GRID_STABLE the order inside a cell is
+ * unspecified.  All seven arrays must be distinct. */
 int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
                uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, void *ws,
                unsigned flags, const grid_params *p, void *stream);
