@@ -1,5 +1,5 @@
 // Device routines of the stable mode's segment sort, shared by the segment-sort
-// kernels and the fused build.
+// kernels and the single-launch builds (fused and bucketed).
 //
 // "Construir el índice de la rejilla con un prefix sum" (§El orden dentro de
 // la celda): sorting every cell's segment of ordenado by particle index gives
