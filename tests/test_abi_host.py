@@ -43,13 +43,13 @@ def test_workspace_bytes(L):
     p = P(L, 1_000_000, (128, 128, 128), cs=0.078125)
     tiles = (128 ** 3 + 8191) // 8192       # scan tiles of 8192 cells
     r256 = lambda b: (b + 255) // 256 * 256                     # noqa: E731
-    # header, look-back words, per-CTA chunk sums (up to 4096 CTAs), per-particle slots,
-    # per-cell counters of the fused build; then the bucketed build's tables
-    # (totals of up to 8192 buckets in 8 lanes each, bucket
-    # bases) and its (cell, particle) pairs
-    assert L.grid_workspace_bytes(p, 0) == (256 + r256(tiles * 8) + r256(4096 * 4) + r256(4 * 1_000_000)
-                                            + r256(4 * 128 ** 3) + r256(4 * 8 * 8192) + r256(4 * 8192)
-                                            + r256(8 * 1_000_000))
+    # The arrays that stay zero between calls, at offsets that do not depend on
+    # the particle count: header, bucket totals (8192 buckets x 8 lane words),
+    # look-back words, per-cell counters.  Then scratch: per-CTA chunk sums (up
+    # to 4096 CTAs), bucket bases, per-particle slots and (cell, particle) pairs.
+    fixed = 256 + r256(4 * 8 * 8192)
+    assert L.grid_workspace_bytes(p, 0) == (fixed + r256(tiles * 8) + r256(4 * 128 ** 3) + r256(4096 * 4)
+                                            + r256(4 * 8192) + r256(4 * 1_000_000) + r256(8 * 1_000_000))
     stable = L.grid_workspace_bytes(p, L.GRID_STABLE)
     assert stable >= L.grid_workspace_bytes(p, 0) + 4 * 1_000_000
     assert L.grid_workspace_bytes(p, 2) == 0            # unknown flag
@@ -57,7 +57,7 @@ def test_workspace_bytes(L):
     bad.celdas = 7
     assert L.grid_workspace_bytes(bad, 0) == 0
     tiny = P(L, 0, (1, 1, 1), cs=1.0)
-    assert L.grid_workspace_bytes(tiny, 0) == 512 + 4096 * 4 + 256
+    assert L.grid_workspace_bytes(tiny, 0) == fixed + 256 + 256 + 4096 * 4 + 4 * 8192
 
 
 def test_error_strings(L):

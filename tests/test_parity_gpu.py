@@ -139,6 +139,28 @@ def test_input_already_in_cell_order(ug, oracle_lib, name, stable):
     _check(ug, oracle_lib, rows, s.dims, s.origin, s.cell_size, stable)
 
 
+def test_one_workspace_for_many_sizes(ug, oracle_lib):
+    """A workspace sized for the largest call serves smaller ones (fewer
+    particles, fewer cells, stable or not) in any order: the arrays that must
+    be zero between calls sit where every size finds them."""
+    big = ug.make_params(1_000_000, (128,) * 3, (-5.0,) * 3, 0.078125)
+    ws = torch.zeros(ug.grid_workspace_bytes(big, ug.GRID_STABLE), dtype=torch.uint8, device="cuda")
+    cases = [
+        (1_000_000, (128,) * 3, 0, 1), (300_000, (128,) * 3, 0, 2), (1_000_000, (128,) * 3, ug.GRID_STABLE, 3),
+        (50_000, (64,) * 3, 0, 4), (1_000_000, (16,) * 3, 0, 5), (777_777, (100, 128, 90), ug.GRID_STABLE, 6),
+        (1_000_000, (128,) * 3, 0, 7),
+    ]
+    for n, dims, flags, seed in cases:
+        cs = np.float32(10.0 / dims[0])
+        rows = scenes.uniform_particles(n, 1000 + seed)
+        p = ug.make_params(n, dims, (-5.0,) * 3, cs)
+        b = ug.GridBuffers.allocate(p, flags)
+        b.ws = ws
+        got = gpu_build(ug, rows, dims, (-5.0,) * 3, cs, flags, bufs=b, params=p)
+        ref = oracle_lib.build(rows, dims, (-5.0,) * 3, cs)
+        assert_matches_oracle(oracle_lib, rows, got, ref, flags != 0)
+
+
 # ---------------------------------------------------------------- one entry point at a time
 
 def test_phases_one_by_one(ug, oracle_lib):

@@ -10,25 +10,28 @@ namespace ugrid {
 
 static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// The arrays that must be zero between calls come first, at offsets that do
+// not depend on the particle count: the bucket totals (fixed size), the scan's
+// look-back words and the counters (both sized by the cell count, so a call
+// with fewer cells finds its words inside the ones the previous call left
+// zero).  Scratch arrays sized by the particle count follow.
 WsLayout ws_layout(uint64_t n, uint64_t cells, unsigned flags) {
     WsLayout l{};
     size_t off = kHeaderBytes;
+    l.bucket_total = off;
+    off = round_up(off + kBucketMaxCount * kBucketLanes * sizeof(uint32_t), 256);
     l.tile_status = off;
     off = round_up(off + scan_tiles(cells) * sizeof(unsigned long long), 256);
-    l.chunk_sums = off;
-    off = round_up(off + kFusedMaxCtas * sizeof(uint32_t), 256);
-    l.slots = off;
-    off = round_up(off + n * sizeof(uint32_t), 256);
     l.counts = off;
     off = round_up(off + cells * sizeof(uint32_t), 256);
-    if (n != 0) {
-        l.bucket_total = off;
-        off = round_up(off + kBucketMaxCount * kBucketLanes * sizeof(uint32_t), 256);
-        l.bucket_base = off;
-        off = round_up(off + kBucketMaxCount * sizeof(uint32_t), 256);
-        l.pairs = off;
-        off = round_up(off + n * 2 * sizeof(uint32_t), 256);
-    }
+    l.chunk_sums = off;
+    off = round_up(off + kFusedMaxCtas * sizeof(uint32_t), 256);
+    l.bucket_base = off;
+    off = round_up(off + kBucketMaxCount * sizeof(uint32_t), 256);
+    l.slots = off;
+    off = round_up(off + n * sizeof(uint32_t), 256);
+    l.pairs = off;
+    off = round_up(off + n * 2 * sizeof(uint32_t), 256);
     if (flags & GRID_STABLE) {
         l.stable_queue = off;
         off = round_up(off + segment_queue_capacity(n, cells) * sizeof(uint32_t), 256);
