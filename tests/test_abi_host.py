@@ -44,10 +44,10 @@ def test_workspace_bytes(L):
     tiles = (128 ** 3 + 8191) // 8192       # scan tiles of 8192 cells
     r256 = lambda b: (b + 255) // 256 * 256                     # noqa: E731
     # The arrays that stay zero between calls, at offsets that do not depend on
-    # the particle count: header, bucket totals (8192 buckets x 8 lane words),
+    # the particle count: header (alone in 4 KB), bucket totals (8192 buckets x 8 lane words),
     # look-back words, per-cell counters.  Then scratch: per-CTA chunk sums (up
     # to 4096 CTAs), bucket bases, per-particle slots and (cell, particle) pairs.
-    fixed = 256 + r256(4 * 8 * 8192)
+    fixed = 4096 + r256(4 * 8 * 8192)   # the header padded to 4 KB
     assert L.grid_workspace_bytes(p, 0) == (fixed + r256(tiles * 8) + r256(4 * 128 ** 3) + r256(4096 * 4)
                                             + r256(4 * 8192) + r256(4 * 1_000_000) + r256(8 * 1_000_000))
     stable = L.grid_workspace_bytes(p, L.GRID_STABLE)
