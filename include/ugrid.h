@@ -108,11 +108,13 @@ typedef struct grid_ws_header {
     uint32_t scan_done;    /* tiles finished by the running scan; 0 between calls */
     uint32_t stable_big;   /* cells queued for the long-segment sort; 0 between calls */
     uint32_t stable_done;  /* CTAs finished by the running long-segment sort; 0 between calls */
-    uint32_t bar_count;    /* grid-barrier arrivals of the running single-launch build; 0 between calls */
     uint32_t bar_exit;     /* CTAs that finished the running single-launch build; 0 between calls */
     uint32_t counts_clean; /* cells of the fused build's counter array known to be zero */
     uint32_t buckets_clean; /* 1 when the bucketed build's per-bucket totals are all zero */
-    uint32_t reserved[55];
+    uint32_t reserved0[24]; /* the words above fill the first 128 bytes */
+    uint32_t bar_count;    /* grid-barrier arrivals of the running single-launch build; 0 between
+                            * calls.  Alone in its 128-byte line: every CTA polls it. */
+    uint32_t reserved[31];
 } grid_ws_header;
 
 /* Bytes of device workspace the calls below need for these params and flags
