@@ -195,6 +195,21 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
                uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, void *ws,
                unsigned flags, const grid_params *p, void *stream);
 
+/* grid_build from and to host memory, all on `stream`: origen_host (N records)
+ * is copied into the device array origen, the grid is built exactly as by
+ * grid_build, then destino and inicios are copied back into destino_host
+ * (N records) and inicios_host (C+1 words).  The host arrays should be
+ * page-locked (cudaHostAlloc / cudaHostRegister) for the copies to be
+ * asynchronous; they must not overlap each other.  The device arrays follow
+ * grid_build's rules.  The host results are complete once the stream has run
+ * (synchronise it, or wait on an event recorded after the call).  Returns
+ * GRID_EINVAL for a null host array when N > 0 (inicios_host always), else
+ * what the copies and grid_build return. */
+int grid_build_host(const ugrid_particula *origen_host, ugrid_particula *destino_host, uint32_t *inicios_host,
+                    ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos, uint32_t *celdaDe,
+                    uint32_t *inicios, uint32_t *ordenado, void *ws, unsigned flags, const grid_params *p,
+                    void *stream);
+
 /* Exclusive scan for callers that cannot allocate device memory; the pages
  * have no counterpart to it.  It computes exactly what grid_scan computes
  * (inicios[0] = 0, inicios[c+1] = inicios[c] + conteos[c], inicios[C] = N),

@@ -202,3 +202,22 @@ def test_morton_accepts_power_of_two_sides(L):
         assert L.grid_workspace_bytes(p, 0) > 0, dims
     p = L.make_params(10, (4, 4, 6), (0.0, 0.0, 0.0), 1.0, order=L.GRID_ORDER_MORTON)
     assert L.grid_workspace_bytes(p, 0) == 0
+
+
+def test_build_host_checks_host_arrays(L):
+    """grid_build_host rejects missing or overlapping host arrays, and bad
+    device arrays, before anything is enqueued."""
+    p = P(L)
+    bp = ctypes.byref(p)
+    f = FAKE
+    dev = [f + (k << 30) for k in range(3, 10)]      # origen .. ws, all distinct and aligned
+    h = 0x100000000                                  # host addresses, never dereferenced
+    call = lambda oh, dh, ih, d=dev: _call(L, "grid_build_host", oh, dh, ih, *d, 0, bp, None)  # noqa: E731
+    assert call(None, h + (1 << 24), h + (2 << 24)) == EINVAL          # no origen_host
+    assert call(h, None, h + (2 << 24)) == EINVAL                      # no destino_host
+    assert call(h, h + (1 << 24), None) == EINVAL                      # no inicios_host
+    assert call(h, h + 64, h + (2 << 24)) == EINVAL                    # destino_host inside origen_host
+    assert call(h, h + (1 << 24), h + (1 << 24) + 32) == EINVAL        # inicios_host inside destino_host
+    bad = list(dev)
+    bad[0] = dev[0] + 8                                                 # misaligned device origen
+    assert call(h, h + (1 << 24), h + (2 << 24), bad) == EINVAL

@@ -161,6 +161,28 @@ def test_one_workspace_for_many_sizes(ug, oracle_lib):
         assert_matches_oracle(oracle_lib, rows, got, ref, flags != 0)
 
 
+@pytest.mark.parametrize("stable", [False, True], ids=["atomic", "stable"])
+def test_build_from_host_memory(ug, oracle_lib, stable):
+    """grid_build_host: pinned host records in, destino and inicios back in
+    pinned host memory, all on one stream."""
+    s = scenes.SCENES["headline"]
+    rows = s.particles()
+    flags = ug.GRID_STABLE if stable else 0
+    p = ug.make_params(s.n, s.dims, s.origin, s.cell_size)
+    b = ug.GridBuffers.allocate(p, flags)
+    host_in = torch.from_numpy(rows).pin_memory()
+    host_dest = torch.empty((s.n, 8), dtype=torch.float32).pin_memory()
+    host_inicios = torch.empty(s.cells + 1, dtype=torch.int32).pin_memory()
+    dev_in = torch.empty((s.n, 8), dtype=torch.float32, device="cuda")
+    ug.grid_build_host(host_in, host_dest, host_inicios, dev_in, b.destino, b.conteos, b.celdaDe, b.inicios,
+                       b.ordenado, b.ws, p, flags)
+    torch.cuda.synchronize()
+    got = {"status": ug.grid_status(b.ws), "conteos": to_u32(b.conteos), "celdaDe": to_u32(b.celdaDe),
+           "inicios": host_inicios.numpy().view(np.uint32), "ordenado": to_u32(b.ordenado),
+           "destino": host_dest.numpy()}
+    assert_matches_oracle(oracle_lib, rows, got, oracle_lib.build(rows, s.dims, s.origin, s.cell_size), stable)
+
+
 # ---------------------------------------------------------------- one entry point at a time
 
 def test_phases_one_by_one(ug, oracle_lib):

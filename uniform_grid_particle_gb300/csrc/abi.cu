@@ -287,6 +287,42 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
     return cuda_code(e);
 }
 
+int grid_build_host(const ugrid_particula *origen_host, ugrid_particula *destino_host, uint32_t *inicios_host,
+                    ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos, uint32_t *celdaDe,
+                    uint32_t *inicios, uint32_t *ordenado, void *ws, unsigned flags, const grid_params *p,
+                    void *stream) {
+    if (!check_params(p, nullptr)) return GRID_EINVAL;
+    const uint64_t n = p->conteo, c = p->celdas;
+    if (inicios_host == nullptr || (n != 0 && (origen_host == nullptr || destino_host == nullptr)))
+        return GRID_EINVAL;
+    const Span host[] = {{origen_host, n * kRecord}, {destino_host, n * kRecord}, {inicios_host, (c + 1) * 4}};
+    if (!disjoint(host, 3)) return GRID_EINVAL;
+    // grid_build checks the device arrays before anything is enqueued; the
+    // copy in goes first only once they have passed.
+    Geometry g;
+    const WsLayout l = ws_layout(n, c, flags);
+    if (!check_params(p, &g) || (flags & ~GRID_STABLE) || !array_ok(origen, n, 16) || !array_ok(destino, n, 16) ||
+        !array_ok(conteos, c, 16) || !array_ok(celdaDe, n, 4) || !array_ok(inicios, c + 1, 16) ||
+        !array_ok(ordenado, n, 4) || !array_ok(ws, l.total, 256))
+        return GRID_EINVAL;
+    const Span dev[] = {{origen, n * kRecord}, {destino, n * kRecord}, {conteos, c * 4},
+                        {celdaDe, n * 4},      {inicios, (c + 1) * 4}, {ordenado, n * 4},
+                        {ws, l.total}};
+    if (!disjoint(dev, 7)) return GRID_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n != 0) {
+        const cudaError_t e = cudaMemcpyAsync(origen, origen_host, n * kRecord, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_code(e);
+    }
+    const int r = grid_build(origen, destino, conteos, celdaDe, inicios, ordenado, ws, flags, p, stream);
+    if (r != GRID_OK) return r;
+    if (n != 0) {
+        const cudaError_t e = cudaMemcpyAsync(destino_host, destino, n * kRecord, cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return cuda_code(e);
+    }
+    return cuda_code(cudaMemcpyAsync(inicios_host, inicios, (c + 1) * 4, cudaMemcpyDeviceToHost, st));
+}
+
 int grid_reorder_many(const uint32_t *ordenado, const grid_array *arrays, uint32_t count, void *ws,
                       const grid_params *p, void *stream) {
     if (!check_params(p, nullptr) || arrays == nullptr || count == 0 || count > (uint32_t)kMaxArrays)

@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "grid_scatter": ([vp, vp, vp, vp, u, vp, pp, vp], ctypes.c_int),
             "grid_reorder": ([vp, vp, vp, vp, pp, vp], ctypes.c_int),
             "grid_build": ([vp, vp, vp, vp, vp, vp, vp, u, pp, vp], ctypes.c_int),
+            "grid_build_host": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, u, pp, vp], ctypes.c_int),
             "grid_status": ([vp, vp], ctypes.c_int),
             "grid_scan_noalloc": ([vp, vp, pp, vp], ctypes.c_int),
             "grid_diagnostics": ([vp, ctypes.c_uint32, vp, pp, vp], ctypes.c_int),
@@ -198,6 +199,31 @@ def grid_build(origen, destino, conteos, celdaDe, inicios, ordenado, ws, p: grid
                             _u32(conteos, "conteos", p.celdas), _u32(celdaDe, "celdaDe", p.conteo),
                             _u32(inicios, "inicios", p.celdas + 1), _u32(ordenado, "ordenado", p.conteo),
                             _ws(ws), flags, ctypes.byref(p), _stream(stream)), "grid_build")
+
+
+def _host(t, name, numel, dtypes):
+    """A CPU tensor's data pointer (page-locked memory keeps the copies asynchronous)."""
+    if t is None:
+        if numel == 0:
+            return None
+        raise ValueError(f"{name} is required")
+    if t.is_cuda or t.dtype not in dtypes or not t.is_contiguous() or t.numel() < numel:
+        raise ValueError(f"{name} must be a contiguous CPU tensor of {dtypes} with at least {numel} elements")
+    return t.data_ptr()
+
+
+def grid_build_host(origen_host, destino_host, inicios_host, origen, destino, conteos, celdaDe, inicios, ordenado,
+                    ws, p: grid_params, flags: int = 0, stream=None) -> None:
+    """grid_build between host arrays: origen_host is copied to origen, the
+    grid is built, destino and inicios are copied back, all on the stream."""
+    n, c = int(p.conteo), int(p.celdas)
+    _check(lib().grid_build_host(_host(origen_host, "origen_host", 8 * n, (torch.float32,)),
+                                 _host(destino_host, "destino_host", 8 * n, (torch.float32,)),
+                                 _host(inicios_host, "inicios_host", c + 1, _U32_DTYPES),
+                                 _parts(origen, "origen", n), _parts(destino, "destino", n),
+                                 _u32(conteos, "conteos", c), _u32(celdaDe, "celdaDe", n),
+                                 _u32(inicios, "inicios", c + 1), _u32(ordenado, "ordenado", n),
+                                 _ws(ws), flags, ctypes.byref(p), _stream(stream)), "grid_build_host")
 
 
 def grid_scan_noalloc(conteos, inicios, p: grid_params, stream=None) -> None:
