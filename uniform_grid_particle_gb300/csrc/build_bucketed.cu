@@ -182,7 +182,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     uint32_t *s_place = s_who + kBucketCap;                                           // u32[kBucketCap]
     uint32_t *s_cell = s_order, *s_rank = s_order + kCacheMax;  // phase A's cache, over the three buffers
     __shared__ uint32_t s_red[kWarps];
-    __shared__ uint32_t s_rows[kScanVecs][kWarps];
+    __shared__ uint32_t s_rows[kScanVecs + 1][kWarps];  // + the rows' totals
     __shared__ uint32_t s_clean, s_bclean, s_base, s_count, s_nlong;
     __shared__ uint32_t s_long[kLongMax];  // stable mode: cells of the bucket with more than 32 particles
     const uint32_t tid = threadIdx.x;

@@ -73,7 +73,7 @@ build_fused_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch ws
     __shared__ uint32_t s_red[kWarps];
     __shared__ uint4 s_held[kScanVecs][kThreads];  // grouping table, then this CTA's chunk of counts (32 KB)
     __shared__ uint32_t s_clean;
-    __shared__ uint32_t s_rows[kScanVecs][kWarps];
+    __shared__ uint32_t s_rows[kScanVecs + 1][kWarps];  // + the rows' totals
     const uint32_t tid = threadIdx.x;
     const uint32_t ctas = gridDim.x;
     uint32_t passed = 0;  // grid barriers passed (thread 0)

@@ -103,7 +103,12 @@ __device__ inline uint32_t block_sum(uint32_t v, uint32_t *s_red) {
 
 // Exclusive scans of kScanVecs rows at once: row q holds one value per
 // thread (t[q]); excl[q] receives the thread's exclusive prefix within row q
-// and rows[q] the row's total.  Two __syncthreads for all rows.
+// and rows[q] the row's total.  Each warp scans its lanes with shuffles; warp
+// 0 then scans the warps' totals of every row (16 lanes per row) and leaves
+// the prefixes in s_rows, row kScanVecs holding the rows' totals.  Three
+// __syncthreads for all rows.
+static_assert(32 % kWarps == 0 && (kScanVecs * kWarps) % 32 == 0 && kScanVecs <= kWarps,
+              "warp 0 scans the warp totals of all rows in segments of kWarps lanes");
 __device__ __forceinline__ void rows_exclusive_scan(const uint32_t (&t)[kScanVecs],
                                                     uint32_t (&excl)[kScanVecs],
                                                     uint32_t (&rows)[kScanVecs],
@@ -125,17 +130,32 @@ __device__ __forceinline__ void rows_exclusive_scan(const uint32_t (&t)[kScanVec
         for (int q = 0; q < kScanVecs; ++q) s_rows[q][warp] = incl[q];
     }
     __syncthreads();
+    if (warp == 0) {
+        // Entry e = j * 32 + lane of the flattened [kScanVecs][kWarps] table.
+        constexpr int kPer = kScanVecs * kWarps / 32;
+        const uint32_t seg = lane % kWarps;
+        uint32_t x[kPer], v[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) v[j] = x[j] = (&s_rows[0][0])[j * 32 + lane];
+#pragma unroll
+        for (int o = 1; o < kWarps; o <<= 1) {
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const uint32_t up = __shfl_up_sync(0xffffffffu, v[j], o, kWarps);
+                if (seg >= (uint32_t)o) v[j] += up;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            (&s_rows[0][0])[j * 32 + lane] = v[j] - x[j];
+            if (seg == kWarps - 1) s_rows[kScanVecs][(j * 32 + lane) / kWarps] = v[j];
+        }
+    }
+    __syncthreads();
 #pragma unroll
     for (int q = 0; q < kScanVecs; ++q) {
-        uint32_t before = 0, total = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const uint32_t x = s_rows[q][w];
-            before += (uint32_t)w < warp ? x : 0u;
-            total += x;
-        }
-        excl[q] = before + incl[q] - t[q];
-        rows[q] = total;
+        excl[q] = s_rows[q][warp] + incl[q] - t[q];
+        rows[q] = s_rows[kScanVecs][q];
     }
     __syncthreads();
 }
