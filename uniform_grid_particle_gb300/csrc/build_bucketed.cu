@@ -201,6 +201,10 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     particle_range(a.n, p_lo, p_hi);
     const uint32_t mine = (uint32_t)(p_hi - p_lo);
     const bool cached = mine <= kCacheMax;
+    // Phase C can then write the pairs bucket by bucket (runs of consecutive
+    // positions) when the table has room for a second copy of the histogram
+    // and for the CTA's particles in bucket order.
+    const bool grouped = cached && B <= 4u * kThreads && 2u * B + mine <= kBucketMaxCount;
 
     UGRID_PHASE_MARK(0);
     if (!s_bclean) {
@@ -243,6 +247,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     // the atomic's old value is the offset, and the lane words end as totals.
     for (uint32_t b = tid; b < B; b += kThreads) {
         const uint32_t m = s_table[b];
+        if (grouped) s_table[B + b] = m;  // the histogram, kept for phase C
         if (m) s_table[b] = atomicAdd(bk.total + (uint64_t)b * kBucketLanes + blockIdx.x % kBucketLanes, m);
     }
     UGRID_PHASE_END(1);
@@ -305,7 +310,49 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     if (heavy) {
         atomic_path<kStable>(a, g, hdr, ws, bk, s_clean != 0u, passed, p_lo, p_hi, s_held, s_red, s_rows);
     } else {
-        if (cached) {
+        if (grouped) {
+            // The CTA's particles in bucket order first (its histogram
+            // scanned, plus each particle's rank in its bucket), so that the
+            // pairs leave as runs of consecutive positions, one run per
+            // bucket, rather than one scattered 8-byte write per particle.
+            uint32_t *s_from = s_table + B, *s_stage = s_table + 2u * B;
+            {
+                uint32_t h[kScanVecs], excl[kScanVecs], rows[kScanVecs];
+                const uint32_t b0 = 4u * tid;
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) w[e] = b0 + e < B ? s_from[b0 + e] : 0u;
+                h[0] = w[0] + w[1] + w[2] + w[3];
+#pragma unroll
+                for (int q = 1; q < kScanVecs; ++q) h[q] = 0u;
+                rows_exclusive_scan(h, excl, rows, s_rows);
+                uint32_t f = excl[0];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (b0 + e < B) s_from[b0 + e] = f;
+                    f += w[e];
+                }
+            }
+            __syncthreads();
+            for (uint32_t k = tid; k < mine; k += kThreads) {
+                const uint32_t at = s_from[bucket_of(s_cell[k], bk)] + s_rank[k];
+                if (at < mine)
+                    s_stage[at] = k;
+                else
+                    record_status(&hdr->status, kStatusBounds);
+            }
+            __syncthreads();
+            for (uint32_t j = tid; j < mine; j += kThreads) {
+                const uint32_t k = s_stage[j];
+                if (k >= mine) continue;
+                const uint32_t c = s_cell[k], b = bucket_of(c, bk);
+                const uint32_t q = s_table[b] + (j - s_from[b]);
+                if (q < a.n)
+                    bk.pairs[q] = make_uint2(c, (uint32_t)(p_lo + k));
+                else
+                    record_status(&hdr->status, kStatusBounds);
+            }
+        } else if (cached) {
             // Phase A kept each particle's cell and its rank among this CTA's
             // particles of its bucket: the pair's place needs no atomic.
             for (uint32_t k = tid; k < mine; k += kThreads) {
