@@ -281,7 +281,11 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
         most = __reduce_max_sync(0xffffffffu, most);
         if (lane_id() == 0) s_red[tid >> 5] = most;
         uint32_t excl[kScanVecs], rows[kScanVecs];
-        rows_exclusive_scan(t, excl, rows, s_rows);  // its barriers also publish s_red
+        // its barriers also publish s_red; up to 4 * kThreads buckets fill one row
+        if (B <= 4u * kThreads)
+            rows_exclusive_scan<1>(t, excl, rows, s_rows);
+        else
+            rows_exclusive_scan(t, excl, rows, s_rows);
         most = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) most = max(most, s_red[w]);
@@ -325,7 +329,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
                 h[0] = w[0] + w[1] + w[2] + w[3];
 #pragma unroll
                 for (int q = 1; q < kScanVecs; ++q) h[q] = 0u;
-                rows_exclusive_scan(h, excl, rows, s_rows);
+                rows_exclusive_scan<1>(h, excl, rows, s_rows);
                 uint32_t f = excl[0];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {

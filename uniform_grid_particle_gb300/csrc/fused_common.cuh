@@ -101,14 +101,15 @@ __device__ inline uint32_t block_sum(uint32_t v, uint32_t *s_red) {
     return t;
 }
 
-// Exclusive scans of kScanVecs rows at once: row q holds one value per
+// Exclusive scans of the first kRows rows at once: row q holds one value per
 // thread (t[q]); excl[q] receives the thread's exclusive prefix within row q
-// and rows[q] the row's total.  Each warp scans its lanes with shuffles; warp
-// 0 then scans the warps' totals of every row (16 lanes per row) and leaves
-// the prefixes in s_rows, row kScanVecs holding the rows' totals.  Three
-// __syncthreads for all rows.
+// and rows[q] the row's total (zero for the rows past kRows).  Each warp
+// scans its lanes with shuffles; warp 0 then scans the warps' totals of every
+// row (kWarps lanes per row) and leaves the prefixes in s_rows, row kScanVecs
+// holding the rows' totals.  Three __syncthreads for all rows.
 static_assert(32 % kWarps == 0 && (kScanVecs * kWarps) % 32 == 0 && kScanVecs <= kWarps,
               "warp 0 scans the warp totals of all rows in segments of kWarps lanes");
+template <int kRows = kScanVecs>
 __device__ __forceinline__ void rows_exclusive_scan(const uint32_t (&t)[kScanVecs],
                                                     uint32_t (&excl)[kScanVecs],
                                                     uint32_t (&rows)[kScanVecs],
@@ -116,27 +117,27 @@ __device__ __forceinline__ void rows_exclusive_scan(const uint32_t (&t)[kScanVec
     const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
     uint32_t incl[kScanVecs];
 #pragma unroll
-    for (int q = 0; q < kScanVecs; ++q) incl[q] = t[q];
+    for (int q = 0; q < kRows; ++q) incl[q] = t[q];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-        for (int q = 0; q < kScanVecs; ++q) {
+        for (int q = 0; q < kRows; ++q) {
             const uint32_t up = __shfl_up_sync(0xffffffffu, incl[q], o);
             if (lane >= (uint32_t)o) incl[q] += up;
         }
     }
     if (lane == 31) {
 #pragma unroll
-        for (int q = 0; q < kScanVecs; ++q) s_rows[q][warp] = incl[q];
+        for (int q = 0; q < kRows; ++q) s_rows[q][warp] = incl[q];
     }
     __syncthreads();
     if (warp == 0) {
         // Entry e = j * 32 + lane of the flattened [kScanVecs][kWarps] table.
-        constexpr int kPer = kScanVecs * kWarps / 32;
+        constexpr int kPer = (kRows * kWarps + 31) / 32;
         const uint32_t seg = lane % kWarps;
         uint32_t x[kPer], v[kPer];
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) v[j] = x[j] = (&s_rows[0][0])[j * 32 + lane];
+        for (int j = 0; j < kPer; ++j) v[j] = x[j] = j * 32 + lane < kRows * kWarps ? (&s_rows[0][0])[j * 32 + lane] : 0u;
 #pragma unroll
         for (int o = 1; o < kWarps; o <<= 1) {
 #pragma unroll
@@ -147,15 +148,17 @@ __device__ __forceinline__ void rows_exclusive_scan(const uint32_t (&t)[kScanVec
         }
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
-            (&s_rows[0][0])[j * 32 + lane] = v[j] - x[j];
-            if (seg == kWarps - 1) s_rows[kScanVecs][(j * 32 + lane) / kWarps] = v[j];
+            if (j * 32 + lane < kRows * kWarps) {
+                (&s_rows[0][0])[j * 32 + lane] = v[j] - x[j];
+                if (seg == kWarps - 1) s_rows[kScanVecs][(j * 32 + lane) / kWarps] = v[j];
+            }
         }
     }
     __syncthreads();
 #pragma unroll
     for (int q = 0; q < kScanVecs; ++q) {
-        excl[q] = s_rows[q][warp] + incl[q] - t[q];
-        rows[q] = s_rows[kScanVecs][q];
+        excl[q] = q < kRows ? s_rows[q][warp] + incl[q] - t[q] : 0u;
+        rows[q] = q < kRows ? s_rows[kScanVecs][q] : 0u;
     }
     __syncthreads();
 }
