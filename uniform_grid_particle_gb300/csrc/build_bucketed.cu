@@ -70,6 +70,9 @@ constexpr int kMaxDevices = 64;
 // Stable mode: cells of one bucket longer than kRegisterMax particles; at most
 // kBucketCap / (kRegisterMax + 1) of them fit in a bucket.
 constexpr uint32_t kLongMax = kBucketCap / (kRegisterMax + 1) + 1;
+// The first buckets a CTA places: phase C keeps their bases and sizes in
+// shared memory when the buckets fit one scan row (any others are read back).
+constexpr uint32_t kOwnMax = 32;
 
 struct BucketScratch {
     uint32_t width;              // cells per bucket
@@ -184,6 +187,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     __shared__ uint32_t s_red[kWarps];
     __shared__ uint32_t s_rows[kScanVecs + 1][kWarps];  // + the rows' totals
     __shared__ uint32_t s_clean, s_bclean, s_base, s_count, s_nlong;
+    __shared__ uint32_t s_own_base[kOwnMax], s_own_count[kOwnMax];
     __shared__ uint32_t s_long[kLongMax];  // stable mode: cells of the bucket with more than 32 particles
     const uint32_t tid = threadIdx.x;
     const uint32_t ctas = gridDim.x;
@@ -251,7 +255,41 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
         if (m) s_table[b] = atomicAdd(bk.total + (uint64_t)b * kBucketLanes + blockIdx.x % kBucketLanes, m);
     }
     UGRID_PHASE_END(1);
-    grid_barrier(hdr, passed);
+    grid_arrive(hdr, passed);
+    if (grouped) {
+        // Phase C writes this CTA's pairs as runs of consecutive positions,
+        // one run per bucket, rather than one scattered 8-byte write per
+        // particle: the CTA's particles in bucket order (its histogram
+        // scanned, plus each particle's rank in its bucket).  This needs no
+        // other CTA, so it runs while the barrier fills.
+        uint32_t *s_from = s_table + B, *s_stage = s_table + 2u * B;
+        {
+            uint32_t h[kScanVecs], excl[kScanVecs], rows[kScanVecs];
+            const uint32_t b0 = 4u * tid;
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = b0 + e < B ? s_from[b0 + e] : 0u;
+            h[0] = w[0] + w[1] + w[2] + w[3];
+#pragma unroll
+            for (int q = 1; q < kScanVecs; ++q) h[q] = 0u;
+            rows_exclusive_scan<1>(h, excl, rows, s_rows);
+            uint32_t f = excl[0];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (b0 + e < B) s_from[b0 + e] = f;
+                f += w[e];
+            }
+        }
+        __syncthreads();
+        for (uint32_t k = tid; k < mine; k += kThreads) {
+            const uint32_t at = s_from[bucket_of(s_cell[k], bk)] + s_rank[k];
+            if (at < mine)
+                s_stage[at] = k;
+            else
+                record_status(&hdr->status, kStatusBounds);
+        }
+    }
+    grid_wait(hdr, passed);
     if (blockIdx.x == 0 && tid == 0) hdr->buckets_clean = 0u;
 
     // ---- C: bucket bases, this CTA's stretch of each bucket, the pairs ------------
@@ -297,11 +335,20 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
                 const uint32_t b0 = 4u * (q * kThreads + tid);
                 const uint32_t f = row_base + excl[q];
                 const uint32_t start[4] = {f, f + v[q].x, f + v[q].x + v[q].y, f + v[q].x + v[q].y + v[q].z};
+                const uint32_t size[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     if (b0 + e < B) {
                         if (blockIdx.x == 0) bk.base[b0 + e] = start[e];
                         s_table[b0 + e] += start[e];  // cursor of this CTA's stretch
+                        if (q == 0 && B <= 4u * kThreads) {
+                            // a bucket this CTA places in phase D: its j-th
+                            const uint32_t j = (b0 + e) / ctas;
+                            if (b0 + e - j * ctas == blockIdx.x && j < kOwnMax) {
+                                s_own_base[j] = start[e];
+                                s_own_count[j] = size[e];
+                            }
+                        }
                     }
                 }
                 row_base += rows[q];
@@ -315,37 +362,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
         atomic_path<kStable>(a, g, hdr, ws, bk, s_clean != 0u, passed, p_lo, p_hi, s_held, s_red, s_rows);
     } else {
         if (grouped) {
-            // The CTA's particles in bucket order first (its histogram
-            // scanned, plus each particle's rank in its bucket), so that the
-            // pairs leave as runs of consecutive positions, one run per
-            // bucket, rather than one scattered 8-byte write per particle.
-            uint32_t *s_from = s_table + B, *s_stage = s_table + 2u * B;
-            {
-                uint32_t h[kScanVecs], excl[kScanVecs], rows[kScanVecs];
-                const uint32_t b0 = 4u * tid;
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) w[e] = b0 + e < B ? s_from[b0 + e] : 0u;
-                h[0] = w[0] + w[1] + w[2] + w[3];
-#pragma unroll
-                for (int q = 1; q < kScanVecs; ++q) h[q] = 0u;
-                rows_exclusive_scan<1>(h, excl, rows, s_rows);
-                uint32_t f = excl[0];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (b0 + e < B) s_from[b0 + e] = f;
-                    f += w[e];
-                }
-            }
-            __syncthreads();
-            for (uint32_t k = tid; k < mine; k += kThreads) {
-                const uint32_t at = s_from[bucket_of(s_cell[k], bk)] + s_rank[k];
-                if (at < mine)
-                    s_stage[at] = k;
-                else
-                    record_status(&hdr->status, kStatusBounds);
-            }
-            __syncthreads();
+            const uint32_t *s_from = s_table + B, *s_stage = s_table + 2u * B;
             for (uint32_t j = tid; j < mine; j += kThreads) {
                 const uint32_t k = s_stage[j];
                 if (k >= mine) continue;
@@ -388,22 +405,29 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
             }
         }
         UGRID_PHASE_END(3);
-        grid_barrier(hdr, passed);
+        grid_arrive(hdr, passed);
+        // The first bucket's cell table is cleared while the barrier fills.
+#pragma unroll
+        for (int q = 0; q < kScanVecs; ++q) s_held[q][tid] = make_uint4(0u, 0u, 0u, 0u);
+        grid_wait(hdr, passed);
 
         // ---- D: each bucket placed by one CTA ---------------------------------
         UGRID_PHASE_MARK(4);
-        for (uint32_t b = blockIdx.x; b < B; b += ctas) {
+        for (uint32_t b = blockIdx.x, j = 0; b < B; b += ctas, ++j) {
             const uint64_t cl = (uint64_t)b * bk.width;
             const uint32_t w = (uint32_t)min((uint64_t)bk.width, a.cells - cl);
             if (tid == 0) {
                 s_nlong = 0u;
-                s_base = bk.base[b];
-                uint32_t unused;
-                s_count = bucket_total(bk.total, b, 0u, unused);
+                if (B <= 4u * kThreads && j < kOwnMax) {
+                    s_base = s_own_base[j];
+                    s_count = s_own_count[j];
+                } else {
+                    s_base = bk.base[b];
+                    uint32_t unused;
+                    s_count = bucket_total(bk.total, b, 0u, unused);
+                }
                 zero_bucket(bk.total, b);  // clean for the next build
             }
-#pragma unroll
-            for (int q = 0; q < kScanVecs; ++q) s_held[q][tid] = make_uint4(0u, 0u, 0u, 0u);
             __syncthreads();
             const uint32_t base = s_base;
             const uint32_t t = base <= a.n ? min(min(s_count, kBucketCap), a.n - base) : 0u;
@@ -512,7 +536,10 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
                     if (src[k] < a.n) store_cs(a.destino + 2 * (uint64_t)base + h, rec[k]);
                 }
             }
-            __syncthreads();  // the tables are cleared for the next bucket
+            __syncthreads();
+            // The cell table, cleared for the next bucket.
+#pragma unroll
+            for (int q = 0; q < kScanVecs; ++q) s_held[q][tid] = make_uint4(0u, 0u, 0u, 0u);
         }
         if (blockIdx.x == 0 && tid == 0) a.inicios[a.cells] = a.n;
     }

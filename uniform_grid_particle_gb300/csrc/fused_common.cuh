@@ -68,13 +68,20 @@ __device__ __forceinline__ void arrive_release(uint32_t *p) {
 // __syncthreads before the arrival makes the CTA's writes visible to thread 0,
 // whose release add publishes them; the acquire loads that see every arrival
 // make the other CTAs' writes visible, and the closing __syncthreads hands
-// them to the whole CTA.
-__device__ inline void grid_barrier(grid_ws_header *hdr, uint32_t &passed) {
+// them to the whole CTA.  A CTA may do work of its own between grid_arrive
+// and grid_wait, as long as that work neither writes what other CTAs read
+// after the barrier nor reads what they write before it.
+__device__ __forceinline__ void grid_arrive(grid_ws_header *hdr, uint32_t &passed) {
     __syncthreads();
     if (threadIdx.x == 0) {
         passed += 1u;
-        const uint32_t target = passed * gridDim.x;
         arrive_release(&hdr->bar_count);
+    }
+}
+
+__device__ inline void grid_wait(grid_ws_header *hdr, uint32_t passed) {
+    if (threadIdx.x == 0) {
+        const uint32_t target = passed * gridDim.x;
         if (load_acquire(&hdr->bar_count) < target) {
             const unsigned long long start = global_ns();
             uint32_t polls = 0;
@@ -87,6 +94,11 @@ __device__ inline void grid_barrier(grid_ws_header *hdr, uint32_t &passed) {
         }
     }
     __syncthreads();
+}
+
+__device__ __forceinline__ void grid_barrier(grid_ws_header *hdr, uint32_t &passed) {
+    grid_arrive(hdr, passed);
+    grid_wait(hdr, passed);
 }
 
 // Block-wide sum (every thread gets it).
