@@ -341,13 +341,16 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
                     if (b0 + e < B) {
                         if (blockIdx.x == 0) bk.base[b0 + e] = start[e];
                         s_table[b0 + e] += start[e];  // cursor of this CTA's stretch
-                        if (q == 0 && B <= 4u * kThreads) {
-                            // a bucket this CTA places in phase D: its j-th
-                            const uint32_t j = (b0 + e) / ctas;
-                            if (b0 + e - j * ctas == blockIdx.x && j < kOwnMax) {
-                                s_own_base[j] = start[e];
-                                s_own_count[j] = size[e];
-                            }
+                    }
+                }
+                // The buckets this CTA places in phase D, blockIdx.x + j * ctas:
+                // their bases and sizes, from the thread that holds them.
+                if (q == 0 && B <= 4u * kThreads) {
+                    for (uint32_t j = 0, bj = blockIdx.x; bj < B && j < kOwnMax; ++j, bj += ctas) {
+                        if ((bj >> 2) == tid) {
+                            const uint32_t e = bj & 3u;
+                            s_own_base[j] = e == 0 ? start[0] : e == 1 ? start[1] : e == 2 ? start[2] : start[3];
+                            s_own_count[j] = e == 0 ? size[0] : e == 1 ? size[1] : e == 2 ? size[2] : size[3];
                         }
                     }
                 }
