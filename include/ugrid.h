@@ -170,10 +170,11 @@ int grid_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cur
 
 /* a5 — gather reorder ("Reordenar por celda y la coalescencia de memoria",
  * §El kernel de reordenación): destino[k] = origen[ordenado[k]] for k < N,
- * whole 32-byte records; writes are contiguous, reads scattered.
+ * whole 32-byte records; writes are contiguous, reads scattered (by the
+ * tensor memory accelerator, four records per copy).
  * origen and destino are distinct, non-overlapping ugrid_particula[N] arrays,
  * 16-byte aligned.  An index >= N sets status bit 1 and that record is not
- * written. */
+ * written.  GRID_ECUDA when the driver offers no tensor-map encoder. */
 int grid_reorder(const uint32_t *ordenado, const ugrid_particula *origen, ugrid_particula *destino,
                  void *ws, const grid_params *p, void *stream);
 

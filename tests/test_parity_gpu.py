@@ -226,6 +226,26 @@ def test_phases_one_by_one(ug, oracle_lib):
     assert np.array_equal(destino.cpu().numpy().view(np.uint32), ref["destino"].view(np.uint32))
 
 
+@pytest.mark.parametrize("n", [1, 3, 127, 128, 129, 1023, 4097, 131073, 1_000_003])
+def test_reorder_sizes(ug, oracle_lib, n):
+    """grid_reorder alone over ragged sizes (partial chunks of 128 records,
+    partial groups of four) and an index list with repeats, against the
+    oracle's gather."""
+    rng = np.random.default_rng(n)
+    rows = rng.standard_normal((n, 8)).astype(np.float32)
+    ordenado = rng.permutation(n).astype(np.uint32)
+    if n > 10:
+        ordenado[rng.integers(0, n, n // 10)] = rng.integers(0, n, n // 10)  # some indices repeat
+    p = ug.make_params(n, (4, 4, 4), (0, 0, 0), 1.0)
+    ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
+    origen = torch.from_numpy(rows).cuda()
+    destino = torch.full_like(origen, float("nan"))
+    ug.grid_reorder(torch.from_numpy(ordenado.view(np.int32)).cuda(), origen, destino, ws, p)
+    torch.cuda.synchronize()
+    assert ug.grid_status(ws) == 0
+    assert np.array_equal(destino.cpu().numpy().view(np.uint32), oracle_lib.reorder(ordenado, rows).view(np.uint32))
+
+
 def test_scan_large_counts(ug, oracle_lib):
     """Counts up to 1000 per cell (totals near 2^31) over a ragged cell count."""
     C = 2_097_152 + 1234

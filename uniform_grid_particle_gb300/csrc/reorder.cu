@@ -5,45 +5,193 @@
 // contiguous and only the reads are scattered (the scatter direction is
 // rejected on that page because scattered writes cost more).
 //
-// Two adjacent threads move one record, 16 bytes each: a warp reads 16 whole
-// 32-byte sectors from scattered places and writes 512 contiguous bytes, so
-// every sector fetched or written is used in full.
+// The records are fetched by the tensor memory accelerator: origen is a 2-D
+// tensor of N rows of eight u32 words, and one tile::gather4 copy brings four
+// whole rows, named by their indices, into shared memory.  Each warp owns a
+// chunk of 128 output positions at a time: every lane reads four entries of
+// ordenado and issues one gather4, an mbarrier counts the chunk's bytes in,
+// and one bulk copy writes the 4 KB chunk to destino.  Two stages per warp
+// keep a chunk in flight while the previous one is written.  No record passes
+// through registers.
+//
+// A chunk holding an index >= N is not gathered: the warp copies its valid
+// records with plain loads and stores, skips the bad ones and sets the bounds
+// status bit.
+#include <cuda.h>
+
+#include <algorithm>
+#include <atomic>
+
 #include "ugrid_internal.cuh"
 
 namespace ugrid {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kItems = 4;  // half-records per thread, loads issued before stores
+constexpr int kWarps = 8;
+constexpr int kStages = 2;
+constexpr uint32_t kChunk = 128;  // records per chunk: four per lane, one gather4 per lane
+constexpr uint32_t kStageBytes = kChunk * sizeof(ugrid_particula);  // 4 KB
+constexpr size_t kStageArea = (size_t)kWarps * kStages * kStageBytes;  // 64 KB
+// After the stages: one mbarrier and one "bad chunk" word per warp and stage.
+constexpr size_t kSmemBytes = kStageArea + (size_t)kWarps * kStages * (sizeof(unsigned long long) + sizeof(uint32_t));
+constexpr int kMaxDevices = 64;
 
-__global__ void __launch_bounds__(kThreads)
-reorder_kernel(const uint32_t *__restrict__ ordenado, const uint4 *__restrict__ origen,
-               uint4 *__restrict__ destino, uint32_t n, uint32_t *status) {
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    const unsigned long long start = global_ns();
+    uint32_t polls = 0;
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((++polls & 63u) == 0 && global_ns() - start > kSpinLimitNs) return false;
+    }
+}
+
+__global__ void __launch_bounds__(32 * kWarps, 2)
+reorder_kernel(const __grid_constant__ CUtensorMap origen_map, const uint32_t *__restrict__ ordenado,
+               const uint4 *__restrict__ origen, uint4 *__restrict__ destino, uint32_t n, uint32_t *status) {
+    extern __shared__ __align__(1024) unsigned char smem[];
     allow_dependent_launch();
     grid_dependency_wait();
-    const uint64_t first = (uint64_t)blockIdx.x * (kThreads * kItems) + threadIdx.x;
-    uint32_t src[kItems];
-#pragma unroll
-    for (int k = 0; k < kItems; ++k) {
-        const uint64_t h = first + (uint64_t)k * kThreads;  // half-record index
-        src[k] = (h >> 1) < n ? __ldg(ordenado + (h >> 1)) : 0u;
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    unsigned char *stage = smem + (size_t)warp * kStages * kStageBytes;
+    unsigned long long *bar = reinterpret_cast<unsigned long long *>(smem + kStageArea) + warp * kStages;
+    uint32_t *bad = reinterpret_cast<uint32_t *>(smem + kStageArea + (size_t)kWarps * kStages * 8) + warp * kStages;
+    if ((smem_addr(smem) & 127u) != 0u) {  // the copies need 128-byte aligned stages
+        if (threadIdx.x == 0) record_status(status, kStatusBounds);
+        return;
     }
-    uint4 v[kItems];
+    if (lane < (uint32_t)kStages)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar + lane)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+
+    const uint32_t chunks = (uint32_t)(((uint64_t)n + kChunk - 1) / kChunk);
+    const uint32_t first = blockIdx.x * kWarps + warp, stride = gridDim.x * kWarps;
+    const uint32_t mine = first < chunks ? (chunks - 1u - first) / stride + 1u : 0u;
+
+    // Chunk i of this warp into stage i % kStages.
+    auto issue = [&](uint32_t i) {
+        const uint32_t s = i % kStages;
+        const uint64_t k0 = (uint64_t)(first + i * stride) * kChunk + 4u * lane;
+        const uint32_t v = k0 < n ? (uint32_t)min((uint64_t)4, n - k0) : 0u;
+        int row[4] = {0, 0, 0, 0};
+        bool lane_bad = false;
+        if (v > 0) {
 #pragma unroll
-    for (int k = 0; k < kItems; ++k) {
-        const uint64_t h = first + (uint64_t)k * kThreads;
-        if ((h >> 1) < n && src[k] < n) v[k] = load_nc_na(origen + 2 * (uint64_t)src[k] + (h & 1));
-    }
-#pragma unroll
-    for (int k = 0; k < kItems; ++k) {
-        const uint64_t h = first + (uint64_t)k * kThreads;
-        if ((h >> 1) < n) {
-            if (src[k] < n)
-                store_cs(destino + h, v[k]);
-            else if ((h & 1) == 0)
-                record_status(status, kStatusBounds);
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t r = __ldg(ordenado + k0 + min((uint32_t)e, v - 1u));
+                lane_bad |= r >= n;
+                row[e] = (int)r;
+            }
+        }
+        const bool chunk_bad = __any_sync(0xffffffffu, lane_bad);
+        const uint32_t lanes = __popc(__ballot_sync(0xffffffffu, v > 0));
+        if (lane_bad) record_status(status, kStatusBounds);
+        if (lane == 0) {
+            bad[s] = chunk_bad ? 1u : 0u;
+            if (chunk_bad)
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar + s)) : "memory");
+            else
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar + s)),
+                             "r"(lanes * 4u * (uint32_t)sizeof(ugrid_particula))
+                             : "memory");
+        }
+        __syncwarp();
+        if (!chunk_bad && v > 0)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(stage + s * kStageBytes +
+                                                                            4u * lane * sizeof(ugrid_particula))),
+                "l"(&origen_map), "r"(0), "r"(row[0]), "r"(row[1]), "r"(row[2]), "r"(row[3]),
+                "r"(smem_addr(bar + s))
+                : "memory");
+    };
+
+    for (uint32_t i = 0; i < min(mine, (uint32_t)kStages); ++i) issue(i);
+    for (uint32_t i = 0; i < mine; ++i) {
+        const uint32_t s = i % kStages;
+        if (!mbar_wait(smem_addr(bar + s), (i / kStages) & 1u)) {
+            if (lane == 0) record_status(status, kStatusTimeout);
+            // Let the other chunk in flight land (again with a limit) before
+            // the CTA leaves.
+            for (uint32_t j = i + 1; j < min(mine, i + kStages); ++j)
+                if (!mbar_wait(smem_addr(bar + j % kStages), (j / kStages) & 1u)) break;
+            break;
+        }
+        const uint64_t k0 = (uint64_t)(first + i * stride) * kChunk;
+        const uint32_t rows = (uint32_t)min((uint64_t)kChunk, n - k0);
+        if (bad[s]) {
+            for (uint32_t h = lane; h < 2u * rows; h += 32u) {
+                const uint32_t src = __ldg(ordenado + k0 + (h >> 1));
+                if (src < n) store_cs(destino + 2 * k0 + h, load_nc_na(origen + 2 * (uint64_t)src + (h & 1u)));
+            }
+        } else if (lane == 0) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(destino + 2 * k0),
+                         "r"(smem_addr(stage + s * kStageBytes)), "r"(rows * (uint32_t)sizeof(ugrid_particula))
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        if (i + kStages < mine) {
+            // The stage is refilled only once its bulk copy has read it.
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+            issue(i + kStages);
         }
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+    static std::atomic<EncodeTiled> fn{nullptr};
+    EncodeTiled f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        f = reinterpret_cast<EncodeTiled>(p);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+std::atomic<int> g_ctas[kMaxDevices];  // grid size per device (0 = not yet known)
+
+cudaError_t reorder_grid(int *ctas) {
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    if (device >= 0 && device < kMaxDevices) {
+        const int cached = g_ctas[device].load(std::memory_order_relaxed);
+        if (cached > 0) {
+            *ctas = cached;
+            return cudaSuccess;
+        }
+    }
+    int sms = 0, per_sm = 0;
+    e = cudaFuncSetAttribute(reorder_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reorder_kernel, 32 * kWarps, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    *ctas = sms * std::min(per_sm, 2);
+    if (device >= 0 && device < kMaxDevices) g_ctas[device].store(*ctas, std::memory_order_relaxed);
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -52,12 +200,25 @@ cudaError_t launch_reorder(const uint32_t *ordenado, const ugrid_particula *orig
                            ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s,
                            bool pdl) {
     if (n == 0) return cudaSuccess;
-    const uint64_t halves = 2ull * n;
-    const uint64_t per_block = (uint64_t)kThreads * kItems;
-    const unsigned blocks = (unsigned)((halves + per_block - 1) / per_block);
-    return launch(reorder_kernel, blocks, kThreads, 0, s, pdl, ordenado,
-                  reinterpret_cast<const uint4 *>(origen), reinterpret_cast<uint4 *>(destino), n,
-                  status);
+    const EncodeTiled encode = encode_tiled();
+    if (encode == nullptr) return cudaErrorNotSupported;
+    // origen as N rows of eight u32 words; a box of one whole row, as gather4 wants.
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {8, n};
+    const cuuint64_t strides[1] = {sizeof(ugrid_particula)};
+    const cuuint32_t box[2] = {8, 1};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<ugrid_particula *>(origen), dims, strides, box,
+               elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    int ctas = 0;
+    const cudaError_t e = reorder_grid(&ctas);
+    if (e != cudaSuccess) return e;
+    const uint64_t chunks = ((uint64_t)n + kChunk - 1) / kChunk;
+    const unsigned grid = (unsigned)std::min<uint64_t>((uint64_t)ctas, (chunks + kWarps - 1) / kWarps);
+    return launch(reorder_kernel, grid, 32 * kWarps, kSmemBytes, s, pdl, map, ordenado,
+                  reinterpret_cast<const uint4 *>(origen), reinterpret_cast<uint4 *>(destino), n, status);
 }
 
 }  // namespace ugrid
