@@ -246,6 +246,26 @@ def test_reorder_sizes(ug, oracle_lib, n):
     assert np.array_equal(destino.cpu().numpy().view(np.uint32), oracle_lib.reorder(ordenado, rows).view(np.uint32))
 
 
+@pytest.mark.parametrize("n", [1, 129, 4096, 1_000_003])
+def test_reorder_runs(ug, oracle_lib, n):
+    """An ordenado made of runs of consecutive indices (input already in
+    cell order, with a few stretches out of order), against the oracle."""
+    rng = np.random.default_rng(n + 7)
+    rows = rng.standard_normal((n, 8)).astype(np.float32)
+    ordenado = np.arange(n, dtype=np.uint32)
+    for _ in range(min(20, n // 64)):
+        a = int(rng.integers(0, n - 32))
+        ordenado[a:a + 32] = ordenado[a:a + 32][::-1].copy()
+    p = ug.make_params(n, (4, 4, 4), (0, 0, 0), 1.0)
+    ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
+    origen = torch.from_numpy(rows).cuda()
+    destino = torch.full_like(origen, float("nan"))
+    ug.grid_reorder(torch.from_numpy(ordenado.view(np.int32)).cuda(), origen, destino, ws, p)
+    torch.cuda.synchronize()
+    assert ug.grid_status(ws) == 0
+    assert np.array_equal(destino.cpu().numpy().view(np.uint32), oracle_lib.reorder(ordenado, rows).view(np.uint32))
+
+
 def test_scan_large_counts(ug, oracle_lib):
     """Counts up to 1000 per cell (totals near 2^31) over a ragged cell count."""
     C = 2_097_152 + 1234

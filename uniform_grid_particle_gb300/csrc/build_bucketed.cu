@@ -73,6 +73,11 @@ constexpr uint32_t kLongMax = kBucketCap / (kRegisterMax + 1) + 1;
 // The first buckets a CTA places: phase C keeps their bases and sizes in
 // shared memory when the buckets fit one scan row (any others are read back).
 constexpr uint32_t kOwnMax = 32;
+// Phase D's gather: records per warp chunk (four per lane) and the stage bytes.
+constexpr uint32_t kGatherChunk = 128;
+constexpr uint32_t kStageBytes = kGatherChunk * sizeof(ugrid_particula);
+static_assert((kWarps / 2) * kStageBytes <= kTableBytes && (kWarps / 2) * kStageBytes <= 2 * kBucketCap * 4,
+              "half the warps stage in the cell table, half in the slot buffers");
 
 struct BucketScratch {
     uint32_t width;              // cells per bucket
@@ -143,6 +148,74 @@ __device__ __forceinline__ uint32_t smem_take(uint32_t *table, bool valid, uint3
     return first + (uint32_t)__popc(peers & lanemask_lt());
 }
 
+// Phase D's record move for one bucket (destino[base + q] = origen[s_order[q]],
+// q < t): each warp takes chunks of 128 positions; every lane names four rows
+// in one tile::gather4 copy into the warp's 4 KB stage, the warp's mbarrier
+// counts them in, and one bulk copy writes the chunk to destino.  A chunk
+// whose rows lie close together is read with 16-byte loads instead.  A
+// chunk naming a row >= n is copied with plain loads, without that row, and
+// sets the bounds bit.  `uses` counts the phases of the warp's mbarrier.
+__device__ __forceinline__ void gather_bucket(const CUtensorMap *map, const BuildArgs &a, const uint32_t *s_order,
+                                              uint32_t t, uint32_t base, unsigned char *stage, uint32_t bar,
+                                              uint32_t &uses, uint32_t *status) {
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t chunks = (t + kGatherChunk - 1u) / kGatherChunk;
+    for (uint32_t c = warp; c < chunks; c += kWarps) {
+        const uint32_t c0 = c * kGatherChunk, rows = min(kGatherChunk, t - c0);
+        const uint32_t q0 = c0 + 4u * lane;
+        const uint32_t v = q0 < t ? min(4u, t - q0) : 0u;
+        int row[4] = {0, 0, 0, 0};
+        bool lane_bad = false;
+        if (v > 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t r = s_order[q0 + min((uint32_t)e, v - 1u)];
+                lane_bad |= r >= a.n;
+                row[e] = (int)r;
+            }
+        }
+        uint4 *dst = a.destino + 2 * ((uint64_t)base + c0);
+        if (__any_sync(0xffffffffu, lane_bad)) {
+            if (lane_bad) record_status(status, kStatusBounds);
+            for (uint32_t h = lane; h < 2u * rows; h += 32u) {
+                const uint32_t src = s_order[c0 + (h >> 1)];
+                if (src < a.n) store_cs(dst + h, load_nc_na(a.origen + 2 * (uint64_t)src + (h & 1u)));
+            }
+            continue;
+        }
+        if (rows_span(row, v) < kClusterRows) {
+            // Rows close together (input already near cell order): 16-byte
+            // loads share their lines; four in flight per lane.
+            for (uint32_t h0 = 0; h0 < 2u * rows; h0 += 4u * 32u) {
+                uint4 r4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t h = h0 + (uint32_t)k * 32u + lane;
+                    if (h < 2u * rows)
+                        r4[k] = load_nc_na(a.origen + 2 * (uint64_t)s_order[c0 + (h >> 1)] + (h & 1u));
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t h = h0 + (uint32_t)k * 32u + lane;
+                    if (h < 2u * rows) store_cs(dst + h, r4[k]);
+                }
+            }
+            continue;
+        }
+        const uint32_t lanes = __popc(__ballot_sync(0xffffffffu, v > 0));
+        if (lane == 0) mbar_arrive_expect(bar, lanes * 4u * (uint32_t)sizeof(ugrid_particula));
+        __syncwarp();
+        if (v > 0) gather4_records(smem_addr(stage + 4u * lane * sizeof(ugrid_particula)), map, row, bar);
+        if (!mbar_wait(bar, uses & 1u)) {
+            if (lane == 0) record_status(status, kStatusTimeout);
+            return;
+        }
+        ++uses;
+        if (lane == 0) bulk_store_wait_read(dst, smem_addr(stage), rows * (uint32_t)sizeof(ugrid_particula));
+        __syncwarp();
+    }
+}
+
 // A bucket too large for one CTA: every CTA takes the atomic path of the
 // fused build from celdaDe on (with its stable tail in stable mode).  Kept out
 // of line so that its registers do not weigh on the bucketed phases.
@@ -176,8 +249,9 @@ __device__ __noinline__ void atomic_path(const BuildArgs a, const Geometry g, gr
 
 template <bool kStable>
 __global__ void __launch_bounds__(kThreads, 2)
-build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch ws, BucketScratch bk) {
-    extern __shared__ uint4 s_dyn[];
+build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs a, Geometry g, grid_ws_header *hdr,
+                      FusedScratch ws, BucketScratch bk) {
+    extern __shared__ __align__(1024) uint4 s_dyn[];
     uint4(*s_held)[kThreads] = reinterpret_cast<uint4(*)[kThreads]>(s_dyn);
     uint32_t *s_table = reinterpret_cast<uint32_t *>(s_dyn);                        // u32[8192], same bytes
     uint32_t *s_order = reinterpret_cast<uint32_t *>(s_dyn + kScanVecs * kThreads);  // u32[kBucketCap]
@@ -188,6 +262,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
     __shared__ uint32_t s_rows[kScanVecs + 1][kWarps];  // + the rows' totals
     __shared__ uint32_t s_clean, s_bclean, s_base, s_count, s_nlong;
     __shared__ uint32_t s_own_base[kOwnMax], s_own_count[kOwnMax];
+    __shared__ __align__(8) unsigned long long s_gbar[kWarps];  // one per warp, phase D's gather
     __shared__ uint32_t s_long[kLongMax];  // stable mode: cells of the bucket with more than 32 particles
     const uint32_t tid = threadIdx.x;
     const uint32_t ctas = gridDim.x;
@@ -198,6 +273,9 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
         s_bclean = *reinterpret_cast<volatile uint32_t *>(&hdr->buckets_clean) != 0u;
     }
     for (uint32_t b = tid; b < kBucketMaxCount; b += kThreads) s_table[b] = 0u;
+    if ((tid & 31u) == 0) mbar_init(smem_addr(&s_gbar[tid >> 5]));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    uint32_t gather_uses = 0;  // phases of this warp's gather mbarrier
     // Nobody touches the long-segment queue of the atomic path before its stable tail.
     if (kStable && blockIdx.x == 0 && tid == 0) hdr->stable_big = 0u;
     __syncthreads();
@@ -521,23 +599,18 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
             UGRID_PHASE_MARK(7);
             for (uint32_t q = tid; q < t; q += kThreads) a.ordenado[base + q] = s_order[q];
             // The bucket's records, gathered in order ("El kernel de
-            // reordenación": destino[k] = origen[ordenado[k]]).
-            unsigned long long last_use;
-            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(last_use));
-            for (uint32_t h0 = 0; h0 < 2 * t; h0 += kThreads * kGatherItems) {
-                uint32_t src[kGatherItems];
-                uint4 rec[kGatherItems];
-#pragma unroll
-                for (int k = 0; k < kGatherItems; ++k) {
-                    const uint32_t h = h0 + (uint32_t)k * kThreads + tid;
-                    src[k] = h < 2 * t ? s_order[h >> 1] : a.n;
-                    if (src[k] < a.n) rec[k] = load_policy(a.origen + 2 * (uint64_t)src[k] + (h & 1), last_use);
-                }
-#pragma unroll
-                for (int k = 0; k < kGatherItems; ++k) {
-                    const uint32_t h = h0 + (uint32_t)k * kThreads + tid;
-                    if (src[k] < a.n) store_cs(a.destino + 2 * (uint64_t)base + h, rec[k]);
-                }
+            // reordenación": destino[k] = origen[ordenado[k]]), through
+            // stages in the cell table (warps 0-7) and the slot buffers
+            // (warps 8-15), both free by now.  The copies write where the
+            // threads wrote: order those writes first.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncthreads();
+            {
+                const uint32_t warp = tid >> 5;
+                unsigned char *stage = reinterpret_cast<unsigned char *>(warp < kWarps / 2 ? s_table : s_who) +
+                                       (size_t)(warp % (kWarps / 2)) * kStageBytes;
+                gather_bucket(&origen_map, a, s_order, t, base, stage, smem_addr(&s_gbar[warp]), gather_uses,
+                              &hdr->status);
             }
             __syncthreads();
             // The cell table, cleared for the next bucket.
@@ -546,6 +619,7 @@ build_bucketed_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch
         }
         if (blockIdx.x == 0 && tid == 0) a.inicios[a.cells] = a.n;
     }
+    if ((tid & 31u) == 0) bulk_wait_all();
     UGRID_PHASE_MARK(6);
     // The last CTA out: every bucket word has been zeroed.
     if (tid == 0 && atomicAdd(&hdr->bar_exit, 1u) == ctas - 1u) {
@@ -606,11 +680,13 @@ cudaError_t launch_build_bucketed(const ugrid_particula *origen, ugrid_particula
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    CUtensorMap map;
+    if (record_tensor_map(origen, n, &map) != cudaSuccess) return cudaErrorNotSupported;
     const FusedScratch ws{chunk_sums, slots, counts, queue, queue_capacity, sort_scratch};
     const BucketScratch bk{plan.width, plan.buckets, plan.magic, total, base, reinterpret_cast<uint2 *>(pairs)};
     const BuildArgs a{reinterpret_cast<const uint4 *>(origen), reinterpret_cast<uint4 *>(destino), conteos, celdaDe,
                       inicios, ordenado, n, cells};
-    return cudaLaunchKernelEx(&cfg, stable ? build_bucketed_kernel<true> : build_bucketed_kernel<false>, a, g, hdr,
+    return cudaLaunchKernelEx(&cfg, stable ? build_bucketed_kernel<true> : build_bucketed_kernel<false>, map, a, g, hdr,
                               ws, bk);
 }
 

@@ -12,13 +12,13 @@
 // ordenado and issues one gather4, an mbarrier counts the chunk's bytes in,
 // and one bulk copy writes the 4 KB chunk to destino.  Two stages per warp
 // keep a chunk in flight while the previous one is written.  No record passes
-// through registers.
+// through registers.  A chunk whose rows lie close together (an ordenado
+// already near order) is read with 16-byte loads instead, which then share
+// lines and sectors.
 //
-// A chunk holding an index >= N is not gathered: the warp copies its valid
-// records with plain loads and stores, skips the bad ones and sets the bounds
-// status bit.
-#include <cuda.h>
-
+// A chunk holding an index >= N is not gathered either: the warp copies its
+// valid records with plain loads and stores, skips the bad ones and sets the
+// bounds status bit.
 #include <algorithm>
 #include <atomic>
 
@@ -32,26 +32,9 @@ constexpr int kStages = 2;
 constexpr uint32_t kChunk = 128;  // records per chunk: four per lane, one gather4 per lane
 constexpr uint32_t kStageBytes = kChunk * sizeof(ugrid_particula);  // 4 KB
 constexpr size_t kStageArea = (size_t)kWarps * kStages * kStageBytes;  // 64 KB
-// After the stages: one mbarrier and one "bad chunk" word per warp and stage.
+// After the stages: one mbarrier and one "plain loads" word per warp and stage.
 constexpr size_t kSmemBytes = kStageArea + (size_t)kWarps * kStages * (sizeof(unsigned long long) + sizeof(uint32_t));
 constexpr int kMaxDevices = 64;
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    const unsigned long long start = global_ns();
-    uint32_t polls = 0;
-    for (;;) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((++polls & 63u) == 0 && global_ns() - start > kSpinLimitNs) return false;
-    }
-}
 
 __global__ void __launch_bounds__(32 * kWarps, 2)
 reorder_kernel(const __grid_constant__ CUtensorMap origen_map, const uint32_t *__restrict__ ordenado,
@@ -62,13 +45,12 @@ reorder_kernel(const __grid_constant__ CUtensorMap origen_map, const uint32_t *_
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     unsigned char *stage = smem + (size_t)warp * kStages * kStageBytes;
     unsigned long long *bar = reinterpret_cast<unsigned long long *>(smem + kStageArea) + warp * kStages;
-    uint32_t *bad = reinterpret_cast<uint32_t *>(smem + kStageArea + (size_t)kWarps * kStages * 8) + warp * kStages;
+    uint32_t *plain = reinterpret_cast<uint32_t *>(smem + kStageArea + (size_t)kWarps * kStages * 8) + warp * kStages;
     if ((smem_addr(smem) & 127u) != 0u) {  // the copies need 128-byte aligned stages
         if (threadIdx.x == 0) record_status(status, kStatusBounds);
         return;
     }
-    if (lane < (uint32_t)kStages)
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar + lane)) : "memory");
+    if (lane < (uint32_t)kStages) mbar_init(smem_addr(bar + lane));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncwarp();
 
@@ -94,24 +76,18 @@ reorder_kernel(const __grid_constant__ CUtensorMap origen_map, const uint32_t *_
         const bool chunk_bad = __any_sync(0xffffffffu, lane_bad);
         const uint32_t lanes = __popc(__ballot_sync(0xffffffffu, v > 0));
         if (lane_bad) record_status(status, kStatusBounds);
+        // A chunk whose rows lie close together is read with 16-byte loads,
+        // which then share lines and sectors, when it is written out.
+        const bool near = !chunk_bad && rows_span(row, v) < kClusterRows;
         if (lane == 0) {
-            bad[s] = chunk_bad ? 1u : 0u;
-            if (chunk_bad)
-                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar + s)) : "memory");
-            else
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar + s)),
-                             "r"(lanes * 4u * (uint32_t)sizeof(ugrid_particula))
-                             : "memory");
+            plain[s] = chunk_bad || near ? 1u : 0u;
+            mbar_arrive_expect(smem_addr(bar + s),
+                               chunk_bad || near ? 0u : lanes * 4u * (uint32_t)sizeof(ugrid_particula));
         }
         __syncwarp();
-        if (!chunk_bad && v > 0)
-            asm volatile(
-                "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-                " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(stage + s * kStageBytes +
-                                                                            4u * lane * sizeof(ugrid_particula))),
-                "l"(&origen_map), "r"(0), "r"(row[0]), "r"(row[1]), "r"(row[2]), "r"(row[3]),
-                "r"(smem_addr(bar + s))
-                : "memory");
+        if (!chunk_bad && !near && v > 0)
+            gather4_records(smem_addr(stage + s * kStageBytes + 4u * lane * sizeof(ugrid_particula)), &origen_map,
+                            row, smem_addr(bar + s));
     };
 
     for (uint32_t i = 0; i < min(mine, (uint32_t)kStages); ++i) issue(i);
@@ -127,10 +103,21 @@ reorder_kernel(const __grid_constant__ CUtensorMap origen_map, const uint32_t *_
         }
         const uint64_t k0 = (uint64_t)(first + i * stride) * kChunk;
         const uint32_t rows = (uint32_t)min((uint64_t)kChunk, n - k0);
-        if (bad[s]) {
-            for (uint32_t h = lane; h < 2u * rows; h += 32u) {
-                const uint32_t src = __ldg(ordenado + k0 + (h >> 1));
-                if (src < n) store_cs(destino + 2 * k0 + h, load_nc_na(origen + 2 * (uint64_t)src + (h & 1u)));
+        if (plain[s]) {
+            // Rows close together, or one out of range: plain loads and
+            // stores, four in flight per lane, skipping any bad row.
+            for (uint32_t h0 = 0; h0 < 2u * rows; h0 += 4u * 32u) {
+                uint32_t src[4];
+                uint4 r4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t h = h0 + (uint32_t)k * 32u + lane;
+                    src[k] = h < 2u * rows ? __ldg(ordenado + k0 + (h >> 1)) : n;
+                    if (src[k] < n) r4[k] = load_nc_na(origen + 2 * (uint64_t)src[k] + (h & 1u));
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (src[k] < n) store_cs(destino + 2 * k0 + h0 + (uint32_t)k * 32u + lane, r4[k]);
             }
         } else if (lane == 0) {
             asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(destino + 2 * k0),
@@ -145,7 +132,7 @@ reorder_kernel(const __grid_constant__ CUtensorMap origen_map, const uint32_t *_
             issue(i + kStages);
         }
     }
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (lane == 0) bulk_wait_all();
     __syncwarp();
 }
 
@@ -196,24 +183,29 @@ cudaError_t reorder_grid(int *ctas) {
 
 }  // namespace
 
-cudaError_t launch_reorder(const uint32_t *ordenado, const ugrid_particula *origen,
-                           ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s,
-                           bool pdl) {
-    if (n == 0) return cudaSuccess;
+cudaError_t record_tensor_map(const ugrid_particula *origen, uint32_t n, CUtensorMap *map) {
     const EncodeTiled encode = encode_tiled();
     if (encode == nullptr) return cudaErrorNotSupported;
-    // origen as N rows of eight u32 words; a box of one whole row, as gather4 wants.
-    CUtensorMap map;
     const cuuint64_t dims[2] = {8, n};
     const cuuint64_t strides[1] = {sizeof(ugrid_particula)};
     const cuuint32_t box[2] = {8, 1};
     const cuuint32_t elem_strides[2] = {1, 1};
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<ugrid_particula *>(origen), dims, strides, box,
+    if (encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<ugrid_particula *>(origen), dims, strides, box,
                elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+cudaError_t launch_reorder(const uint32_t *ordenado, const ugrid_particula *origen,
+                           ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s,
+                           bool pdl) {
+    if (n == 0) return cudaSuccess;
+    CUtensorMap map;
+    cudaError_t e = record_tensor_map(origen, n, &map);
+    if (e != cudaSuccess) return e;
     int ctas = 0;
-    const cudaError_t e = reorder_grid(&ctas);
+    e = reorder_grid(&ctas);
     if (e != cudaSuccess) return e;
     const uint64_t chunks = ((uint64_t)n + kChunk - 1) / kChunk;
     const unsigned grid = (unsigned)std::min<uint64_t>((uint64_t)ctas, (chunks + kWarps - 1) / kWarps);

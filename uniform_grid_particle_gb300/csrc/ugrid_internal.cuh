@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ugrid.h"
@@ -124,6 +125,10 @@ cudaError_t launch_scan(uint32_t *conteos, uint32_t *inicios, uint64_t cells, bo
 cudaError_t launch_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cursor,
                            uint32_t *ordenado, uint32_t n, uint32_t cells, uint32_t *status,
                            cudaStream_t s, bool pdl);
+
+// origen described to the tensor memory accelerator as n rows of eight u32
+// words, with a box of one whole row (the form a tile::gather4 copy reads).
+cudaError_t record_tensor_map(const ugrid_particula *origen, uint32_t n, CUtensorMap *map);
 
 cudaError_t launch_reorder(const uint32_t *ordenado, const ugrid_particula *origen,
                            ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s,
@@ -276,5 +281,74 @@ __device__ __forceinline__ void store_cs(uint4 *p, const uint4 &v) {
                  "r"(v.z), "r"(v.w)
                  : "memory");
 }
+
+// ---- Tensor memory accelerator: a gather of four 32-byte records ----------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+// The one arrival of a phase, expecting `bytes` from copies (0: none).
+__device__ __forceinline__ void mbar_arrive_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Wait for the phase of the given parity to complete; false after 1 s.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    const unsigned long long start = global_ns();
+    uint32_t polls = 0;
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((++polls & 63u) == 0 && global_ns() - start > kSpinLimitNs) return false;
+    }
+}
+
+// Rows r0..r3 of a record tensor map (record_tensor_map) into 128 contiguous
+// bytes at dst (128-byte aligned), counted on the mbarrier.
+__device__ __forceinline__ void gather4_records(uint32_t dst, const CUtensorMap *map, const int (&r)[4],
+                                                uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(map), "r"(0), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(bar)
+        : "memory");
+}
+
+// Rows of a chunk closer together than this are read with plain 16-byte
+// loads, which then share lines and sectors; TMA gathers serve scattered rows.
+constexpr uint32_t kClusterRows = 512;
+
+// The span (largest - smallest) of the warp's rows, lane l holding v of them.
+__device__ __forceinline__ uint32_t rows_span(const int (&row)[4], uint32_t v) {
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        if ((uint32_t)e < v) {
+            lo = min(lo, (uint32_t)row[e]);
+            hi = max(hi, (uint32_t)row[e]);
+        }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    return hi >= lo ? hi - lo : 0u;
+}
+
+// One bulk copy of `bytes` (a multiple of 16) from shared memory to global
+// memory, then wait until the source has been read.
+__device__ __forceinline__ void bulk_store_wait_read(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 }  // namespace ugrid
