@@ -15,11 +15,11 @@
 // and read with single relaxed gpu-scope accesses.  One warp looks back over
 // 256 predecessors per round (8 words per lane), so while all tiles of a
 // 2M-cell grid are in flight a single round reaches tile 0; only that warp
-// polls, which keeps the few L2 lines holding the words from becoming a hot
-// spot.  Every wait gives up after kSpinLimitNs, records kStatusTimeout and
-// carries on with a zero prefix, so a kernel never hangs.  The last CTA to
-// finish zeroes the words and the counters, leaving the workspace ready for
-// the next call.
+// polls, and only the words closer than the nearest inclusive prefix are
+// waited for.  Every wait gives up after kSpinLimitNs, records kStatusTimeout
+// and carries on with a zero prefix, so a kernel never hangs.  Each CTA counts
+// itself out once its look-back is done; the last one zeroes the words and
+// the counters, leaving the workspace ready for the next call.
 //
 // Each tile is four rows of 2048 cells; thread t holds cells 4t..4t+3 of every
 // row, so each row is read and written with fully coalesced 16-byte accesses.
@@ -63,12 +63,15 @@ __device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v) {
 // Exclusive prefix of `tile` from its predecessors' words; called by one full
 // warp.  Word w of lane l is predecessor j - (w*32 + l): the nearest one that
 // shows an inclusive prefix ends the walk, and the tile totals of the closer
-// ones are added to it.
+// ones are added to it.  Only the words closer than that prefix have to be
+// published; pending ones are re-read together, one round trip per poll,
+// with no sleep between polls (a sleep there cost microseconds).
 __device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t tile,
                               uint32_t *status_word) {
     const uint32_t lane = lane_id();
     uint32_t exclusive = 0;
     long long j = (long long)tile - 1;
+    const unsigned long long start = global_ns();
     while (true) {
         unsigned long long s[kLookWords];
 #pragma unroll
@@ -76,39 +79,31 @@ __device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t ti
             const long long idx = j - (long long)(w * 32 + lane);
             s[w] = idx >= 0 ? load_relaxed(tile_status + idx) : kFlagPrefix;
         }
-        // Wait until every word of the window is published, re-reading all the
-        // pending ones together (one round trip per poll, not one per word).
-        bool pending = false;
+        uint32_t nearest;
+        while (true) {
+            // Position (w*32 + lane) of the nearest inclusive prefix in the window.
+            nearest = 0xffffffffu;
 #pragma unroll
-        for (int w = 0; w < kLookWords; ++w) pending |= (s[w] >> 32) == 0;
-        if (__any_sync(kFullMask, pending)) {
-            const unsigned long long start = global_ns();
-            do {
-                __nanosleep(32);
-                pending = false;
+            for (int w = kLookWords - 1; w >= 0; --w)
+                if ((s[w] >> 32) == 2) nearest = (uint32_t)(w * 32) + lane;
+            nearest = __reduce_min_sync(kFullMask, nearest);
+            bool pending = false;
 #pragma unroll
-                for (int w = 0; w < kLookWords; ++w) {
-                    if ((s[w] >> 32) == 0) {
-                        s[w] = load_relaxed(tile_status + (j - (long long)(w * 32 + lane)));
-                        pending |= (s[w] >> 32) == 0;
-                    }
-                }
-                const bool give_up = __shfl_sync(kFullMask, global_ns() - start > kSpinLimitNs, 0);
-                if (give_up && __any_sync(kFullMask, pending)) {
+            for (int w = 0; w < kLookWords; ++w)
+                pending |= (uint32_t)(w * 32) + lane < nearest && (s[w] >> 32) == 0;
+            if (!__any_sync(kFullMask, pending)) break;
+            if (__shfl_sync(kFullMask, global_ns() - start > kSpinLimitNs, 0)) {
 #pragma unroll
-                    for (int w = 0; w < kLookWords; ++w)
-                        if ((s[w] >> 32) == 0) s[w] = kFlagPrefix;  // carry on with a zero prefix
-                    if (lane == 0) record_status(status_word, kStatusTimeout);
-                    pending = false;
-                }
-            } while (__any_sync(kFullMask, pending));
+                for (int w = 0; w < kLookWords; ++w)
+                    if ((s[w] >> 32) == 0) s[w] = kFlagPrefix;  // carry on with a zero prefix
+                if (lane == 0) record_status(status_word, kStatusTimeout);
+                continue;
+            }
+#pragma unroll
+            for (int w = 0; w < kLookWords; ++w)
+                if ((uint32_t)(w * 32) + lane < nearest && (s[w] >> 32) == 0)
+                    s[w] = load_relaxed(tile_status + (j - (long long)(w * 32 + lane)));
         }
-        // Position (w*32 + lane) of the nearest inclusive prefix in the window.
-        uint32_t nearest = 0xffffffffu;
-#pragma unroll
-        for (int w = kLookWords - 1; w >= 0; --w)
-            if ((s[w] >> 32) == 2) nearest = (uint32_t)(w * 32) + lane;
-        nearest = __reduce_min_sync(kFullMask, nearest);
         uint32_t sum = 0;
 #pragma unroll
         for (int w = 0; w < kLookWords; ++w)
@@ -124,7 +119,7 @@ __device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t ti
 // count, which does not touch the workspace; the build's leading memset has
 // already ordered it after any earlier scan on this workspace).
 template <bool kZeroInput>
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(kScanThreads, 2)
 scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, uint32_t tiles,
             grid_ws_header *hdr, unsigned long long *tile_status) {
     __shared__ uint32_t s_tile;
@@ -197,6 +192,9 @@ scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, u
             if (lane == 0) s_prefix = exclusive;
         }
         __syncthreads();
+        // This CTA reads no more look-back words: count it out now, so the
+        // last one can clear them while the others still write inicios.
+        if (tid == 0) s_last = atomicAdd(&hdr->scan_done, 1u) == gridDim.x - 1 ? 1u : 0u;
 
         const uint32_t prefix = s_prefix;
 #pragma unroll
@@ -224,14 +222,10 @@ scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, u
         if (tile == tiles - 1 && tid == 0) inicios[cells] = prefix + tile_total;
     } else if (tid == 0) {
         record_status(&hdr->status, kStatusBounds);  // more CTAs than tiles: a stale ticket
-    }
-
-    // The last CTA out resets the look-back words and the counters.
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
         s_last = atomicAdd(&hdr->scan_done, 1u) == gridDim.x - 1 ? 1u : 0u;
     }
+
+    // The last CTA counted out resets the look-back words and the counters.
     __syncthreads();
     if (s_last) {
         __threadfence();
