@@ -12,57 +12,89 @@
 // kIndirect = false reads parts (= destino) at j directly; kIndirect = true
 // reads parts (= origen) at ordenado[j].  Both give the same rho[k].
 //
-// Linear order: the three x-neighbours of a (dy, dz) row are consecutive
-// cells, so each row is one range of inicios, nine ranges per particle.
-// Morton order: each cell of a row has its own code; codes that follow one
-// another (an even x and the x after it) are merged into one range.
-// Arithmetic in fp32.
+// Linear order: one CTA per run of kTileCells cells of one (y, z) row.  The
+// candidates of all its particles are the particles of 9 rows of cells
+// (dy, dz in -1..1) over the run widened by one cell at each end, and in
+// linear order each of those is one contiguous range of the cell order.  The
+// CTA copies them to shared memory as (x, y, z, masa) once, then every thread
+// walks its particle's 27 cells there: three consecutive cells per row, nine
+// ranges.  A run whose candidates do not fit falls back to the walk below.
+//
+// Morton order, and the fallback: one thread per particle walks its 27 cells
+// in global memory.  In Morton order each cell of a row has its own code;
+// codes that follow one another (an even x and the x after it) are merged
+// into one range.
+//
+// Arithmetic in fp32.  A term is masa * t^3 with t = max(h^2 - r^2, 0), which
+// is the term for r^2 < h^2 and an exact zero otherwise (h^2 - r^2 is formed
+// by fused multiply-adds, so a candidate within an ulp or two of h can fall
+// either way, at a weight of order (ulp of h^2)^3).  Both paths add the same
+// terms in the same order.
 #include "ugrid_internal.cuh"
 
 namespace ugrid {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr uint32_t kTileCells = 16;   // cells of one row per CTA (linear order)
+constexpr uint32_t kStageMax = 4096;  // candidates a CTA keeps in shared memory (64 KB)
+constexpr uint32_t kRowCells = kTileCells + 2;
+// Threads of a tile CTA: one round over its ~kTileCells * 20 own particles at
+// the density of an SPH scene (a second round for a few threads at most).
+constexpr int kTileThreads = 320;
+
+// sum + masa * max(h^2 - r^2, 0)^3, with h^2 - r^2 taken as three fused
+// multiply-adds from h^2 and the product folded into the last add.
+__device__ __forceinline__ float add_term(float sum, float4 q, float px, float py, float pz, float h2) {
+    const float ex = q.x - px, ey = q.y - py, ez = q.z - pz;
+    const float u = fmaf(-ez, ez, fmaf(-ey, ey, fmaf(-ex, ex, h2)));
+    const float t = fmaxf(u, 0.0f);
+    return fmaf(q.w * t * t, t, sum);
+}
+
+// (x, y, z, masa) of the particle at cell-order position j.
+template <bool kIndirect>
+__device__ __forceinline__ float4 candidate(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
+                                            uint32_t j, uint32_t n, bool &bad) {
+    const uint32_t q = kIndirect ? __ldg(ordenado + j) : j;
+    if (q >= n) {
+        bad = true;
+        return make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    const uint4 pq = __ldg(parts + 2 * (uint64_t)q);
+    const float m = __uint_as_float(__ldg(reinterpret_cast<const uint32_t *>(parts) + 8 * (uint64_t)q + 7));
+    return make_float4(__uint_as_float(pq.x), __uint_as_float(pq.y), __uint_as_float(pq.z), m);
+}
 
 template <bool kIndirect>
 __device__ __forceinline__ float accumulate(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
                                             uint32_t a, uint32_t b, float px, float py, float pz, float h2,
-                                            uint32_t n, float sum) {
+                                            uint32_t n, float sum, uint32_t *status) {
     b = min(b, n);
     for (uint32_t j = a; j < b; ++j) {
-        const uint32_t q = kIndirect ? __ldg(ordenado + j) : j;
-        if (q >= n) continue;
-        const uint4 pq = __ldg(parts + 2 * (uint64_t)q);
-        const float ex = __uint_as_float(pq.x) - px;
-        const float ey = __uint_as_float(pq.y) - py;
-        const float ez = __uint_as_float(pq.z) - pz;
-        const float r2 = ex * ex + ey * ey + ez * ez;
-        if (r2 < h2) {
-            const float t = h2 - r2;
-            const float masa =
-                __uint_as_float(__ldg(reinterpret_cast<const uint32_t *>(parts) + 8 * (uint64_t)q + 7));
-            sum += masa * t * t * t;
+        bool bad = false;
+        const float4 q = candidate<kIndirect>(parts, ordenado, j, n, bad);
+        if (bad) {
+            record_status(status, kStatusBounds);
+            continue;
         }
+        sum = add_term(sum, q, px, py, pz, h2);
     }
     return sum;
 }
 
+// The walk in global memory for the particle at cell-order position k.
 template <bool kIndirect, bool kMorton>
-__global__ void __launch_bounds__(kThreads)
-density_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
-               const uint32_t *__restrict__ inicios, Geometry g, float h2, uint32_t n,
-               float *__restrict__ rho, uint32_t *status) {
-    allow_dependent_launch();
-    grid_dependency_wait();
-    const uint64_t k = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
-    if (k >= n) return;
-    const uint32_t self = kIndirect ? __ldg(ordenado + k) : (uint32_t)k;
-    if (self >= n) {
+__device__ __forceinline__ void density_at(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
+                                           const uint32_t *__restrict__ inicios, const Geometry &g, float h2,
+                                           uint32_t n, uint32_t k, float *__restrict__ rho, uint32_t *status) {
+    bool bad = false;
+    const float4 me = candidate<kIndirect>(parts, ordenado, k, n, bad);
+    if (bad) {
         record_status(status, kStatusBounds);
         return;
     }
-    const uint4 me = __ldg(parts + 2 * (uint64_t)self);
-    const float px = __uint_as_float(me.x), py = __uint_as_float(me.y), pz = __uint_as_float(me.z);
+    const float px = me.x, py = me.y, pz = me.z;
     const uint32_t cx = axis_coord(px, g.origin[0], g.inv_cell, g.dims[0]);
     const uint32_t cy = axis_coord(py, g.origin[1], g.inv_cell, g.dims[1]);
     const uint32_t cz = axis_coord(pz, g.origin[2], g.inv_cell, g.dims[2]);
@@ -77,24 +109,138 @@ density_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ord
             if (!kMorton) {
                 const uint64_t row = (uint64_t)g.dims[0] * ((uint64_t)y + (uint64_t)g.dims[1] * (uint64_t)z);
                 sum = accumulate<kIndirect>(parts, ordenado, __ldg(inicios + row + x0), __ldg(inicios + row + x1 + 1),
-                                            px, py, pz, h2, n, sum);
+                                            px, py, pz, h2, n, sum, status);
             } else {
                 uint32_t first = cell_at(x0, (uint32_t)y, (uint32_t)z, g), last = first;
                 for (uint32_t x = x0 + 1; x <= x1; ++x) {
                     const uint32_t c = cell_at(x, (uint32_t)y, (uint32_t)z, g);
                     if (c != last + 1u) {
                         sum = accumulate<kIndirect>(parts, ordenado, __ldg(inicios + first), __ldg(inicios + last + 1),
-                                                    px, py, pz, h2, n, sum);
+                                                    px, py, pz, h2, n, sum, status);
                         first = c;
                     }
                     last = c;
                 }
                 sum = accumulate<kIndirect>(parts, ordenado, __ldg(inicios + first), __ldg(inicios + last + 1), px,
-                                            py, pz, h2, n, sum);
+                                            py, pz, h2, n, sum, status);
             }
         }
     }
     rho[k] = sum;
+}
+
+template <bool kIndirect, bool kMorton>
+__global__ void __launch_bounds__(kThreads)
+density_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
+               const uint32_t *__restrict__ inicios, Geometry g, float h2, uint32_t n,
+               float *__restrict__ rho, uint32_t *status) {
+    allow_dependent_launch();
+    grid_dependency_wait();
+    const uint64_t k = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (k < n) density_at<kIndirect, kMorton>(parts, ordenado, inicios, g, h2, n, (uint32_t)k, rho, status);
+}
+
+// Linear order, one CTA per run of kTileCells cells of one row (see above).
+template <bool kIndirect>
+__global__ void __launch_bounds__(kTileThreads)
+density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
+                    const uint32_t *__restrict__ inicios, Geometry g, float h2, uint32_t n,
+                    float *__restrict__ rho, uint32_t *status) {
+    extern __shared__ float4 s_stage[];                 // kStageMax candidates
+    __shared__ uint32_t s_start[9][kRowCells + 1];      // stage offset of each cell of each row, and the end
+    __shared__ uint32_t s_first[9];                     // cell-order index of each row's first candidate
+    __shared__ uint32_t s_total;
+    allow_dependent_launch();
+    grid_dependency_wait();
+    const uint32_t X = g.dims[0], Y = g.dims[1], Z = g.dims[2];
+    const uint32_t tiles_x = (X + kTileCells - 1) / kTileCells;
+    const uint32_t tx = blockIdx.x % tiles_x, yz = blockIdx.x / tiles_x;
+    const uint32_t y = yz % Y, z = yz / Y;
+    const uint32_t x0 = tx * kTileCells, x1 = min(x0 + kTileCells, X);  // own cells [x0, x1)
+    const uint32_t xa = x0 > 0 ? x0 - 1 : 0u, xb = x1 < X ? x1 : X - 1;  // staged cells [xa, xb]
+    const uint32_t nc = xb - xa + 1;
+    const uint32_t tid = threadIdx.x;
+
+    // Row r = (dz + 1) * 3 + (dy + 1): the cells' starts, relative to the row.
+    for (uint32_t r = tid >> 5, lane = tid & 31u; r < 9; r += kTileThreads / 32) {
+        const int64_t yy = (int64_t)y + (int64_t)(r % 3) - 1, zz = (int64_t)z + (int64_t)(r / 3) - 1;
+        const bool exists = yy >= 0 && yy < (int64_t)Y && zz >= 0 && zz < (int64_t)Z;
+        const uint64_t row = exists ? (uint64_t)X * ((uint64_t)yy + (uint64_t)Y * (uint64_t)zz) : 0;
+        const uint32_t first = exists ? __ldg(inicios + row + xa) : 0u;
+        if (lane <= nc) s_start[r][lane] = exists ? __ldg(inicios + row + xa + lane) - first : 0u;
+        if (lane == 0) s_first[r] = first;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t base = 0;
+        bool fits = true;
+        for (int r = 0; r < 9; ++r) {
+            const uint32_t size = s_start[r][nc];
+            // starts that decrease (inconsistent input) go to the walk, too
+            for (uint32_t c = 1; c <= nc; ++c) fits &= s_start[r][c] >= s_start[r][c - 1];
+            if (size > kStageMax || base + size > kStageMax) fits = false;
+            for (uint32_t c = 0; c <= nc; ++c) s_start[r][c] += base;
+            base += size;
+        }
+        s_total = fits ? base : 0xffffffffu;
+    }
+    __syncthreads();
+    const uint32_t total = s_total;
+    if (total == 0xffffffffu) {
+        // The candidates do not fit: each own particle walks global memory.
+        const uint64_t row = (uint64_t)X * ((uint64_t)y + (uint64_t)Y * (uint64_t)z);
+        const uint32_t k0 = __ldg(inicios + row + x0), k1 = min(__ldg(inicios + row + x1), n);
+        for (uint32_t k = k0 + tid; k < k1; k += kTileThreads)
+            density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, k, rho, status);
+        return;
+    }
+    // Stage the candidates, row by row.
+    for (int r = 0; r < 9; ++r) {
+        const uint32_t base = s_start[r][0], size = s_start[r][nc] - base, first = s_first[r];
+        for (uint32_t j = tid; j < size; j += kTileThreads) {
+            bool bad = first + j >= n;
+            const float4 q = bad ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
+                                 : candidate<kIndirect>(parts, ordenado, first + j, n, bad);
+            if (bad) record_status(status, kStatusBounds);
+            s_stage[base + j] = q;
+        }
+    }
+    __syncthreads();
+    // The own particles: cells [x0, x1) of the centre row (r = 4).
+    const uint32_t own0 = s_start[4][x0 - xa], own1 = s_start[4][x1 - xa];
+    const uint32_t k_of_stage = s_first[4] - s_start[4][0];  // cell-order index = stage index + this
+    for (uint32_t s = own0 + tid; s < own1; s += kTileThreads) {
+        const float4 me = s_stage[s];
+        const uint32_t cx = axis_coord(me.x, g.origin[0], g.inv_cell, X);
+        const uint32_t cy = axis_coord(me.y, g.origin[1], g.inv_cell, Y);
+        const uint32_t cz = axis_coord(me.z, g.origin[2], g.inv_cell, Z);
+        const uint32_t k = k_of_stage + s;
+        if (k >= n) continue;
+        if (cx < x0 || cx >= x1 || cy != y || cz != z) {
+            // Not the cell it is stored in (starts inconsistent with the
+            // positions): the walk in global memory, as for any order.
+            density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, k, rho, status);
+            continue;
+        }
+        const uint32_t lo = (cx > 0 ? cx - 1 : 0u) - xa, hi = (cx + 1 < X ? cx + 1 : cx) - xa;
+        // Four running sums, so that four candidates are in flight at once;
+        // both paths add the same terms in the same order.
+        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll 1
+        for (int r = 0; r < 9; ++r) {
+            const uint32_t a = s_start[r][lo], b = s_start[r][hi + 1];
+            uint32_t j = a;
+            for (; j + 4 <= b; j += 4) {
+                const float4 q0 = s_stage[j], q1 = s_stage[j + 1], q2 = s_stage[j + 2], q3 = s_stage[j + 3];
+                s0 = add_term(s0, q0, me.x, me.y, me.z, h2);
+                s1 = add_term(s1, q1, me.x, me.y, me.z, h2);
+                s2 = add_term(s2, q2, me.x, me.y, me.z, h2);
+                s3 = add_term(s3, q3, me.x, me.y, me.z, h2);
+            }
+            for (; j < b; ++j) s0 = add_term(s0, s_stage[j], me.x, me.y, me.z, h2);
+        }
+        rho[k] = (s0 + s1) + (s2 + s3);
+    }
 }
 
 }  // namespace
@@ -103,10 +249,23 @@ cudaError_t launch_density(const ugrid_particula *parts, const uint32_t *ordenad
                            const uint32_t *inicios, const Geometry &g, float h, uint32_t n,
                            float *rho, uint32_t *status, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)((n + kThreads - 1) / kThreads);
     const float h2 = h * h;
     const uint4 *p4 = reinterpret_cast<const uint4 *>(parts);
     const bool morton = g.order != kOrderLinear;
+    if (!morton) {
+        const uint64_t tiles = (uint64_t)((g.dims[0] + kTileCells - 1) / kTileCells) * g.dims[1] * g.dims[2];
+        const size_t smem = kStageMax * sizeof(float4);
+        if (tiles <= 0x7fffffffull) {
+            cudaError_t e = cudaFuncSetAttribute(ordenado ? density_tile_kernel<true> : density_tile_kernel<false>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            return ordenado ? launch(density_tile_kernel<true>, (unsigned)tiles, kTileThreads, smem, s, true, p4,
+                                     ordenado, inicios, g, h2, n, rho, status)
+                            : launch(density_tile_kernel<false>, (unsigned)tiles, kTileThreads, smem, s, true, p4,
+                                     ordenado, inicios, g, h2, n, rho, status);
+        }
+    }
+    const unsigned blocks = (unsigned)((n + kThreads - 1) / kThreads);
     if (ordenado != nullptr)
         return morton ? launch(density_kernel<true, true>, blocks, kThreads, 0, s, true, p4, ordenado, inicios, g,
                                h2, n, rho, status)
