@@ -37,7 +37,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr uint32_t kTileCells = 16;   // cells of one row per CTA (linear order)
-constexpr uint32_t kStageMax = 4096;  // candidates a CTA keeps in shared memory (64 KB)
+constexpr uint32_t kStageMax = 3584;  // candidates a CTA keeps in shared memory (56 KB: four CTAs per SM)
 constexpr uint32_t kRowCells = kTileCells + 2;
 // Threads of a tile CTA: one round over its ~kTileCells * 20 own particles at
 // the density of an SPH scene (a second round for a few threads at most).
