@@ -570,7 +570,7 @@ def run_gpu(args) -> None:
         # maximum SM clock: 152 SMs x 128 lanes x 2.07 GHz / 7.
         tests_per_s = tests / (neighbour["us_linear_sorted"] * 1e-6) / 1e9
         alu_peak = ALU_LANES * ALU_CLOCK_GHZ / PAIR_TEST_OPS
-        neighbour["roofline"] = {"bound": "alu", "kernel": "density_kernel<0, 0> (linear, reordered records)",
+        neighbour["roofline"] = {"bound": "alu", "kernel": "density_tile_kernel<0> (linear, reordered records)",
                                  "achieved": tests_per_s, "peak": alu_peak, "unit": "Gpair-tests/s",
                                  "frac": tests_per_s / alu_peak, "pair_tests_per_query": int(tests),
                                  "peak_derivation": f"{ALU_LANES} fp32 lanes x {ALU_CLOCK_GHZ} GHz / "
