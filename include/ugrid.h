@@ -118,7 +118,8 @@ typedef struct grid_ws_header {
 } grid_ws_header;
 
 /* Bytes of device workspace the calls below need for these params and flags
- * (the header, the scan's per-tile look-back status words, grid_build's
+ * (the header, the scan's per-tile look-back status words (one per 128-byte
+ * line), grid_build's
  * per-CTA chunk sums, per-particle slots, per-cell counter array, per-bucket
  * totals and first positions and per-particle (cell, particle) pairs and,
  * with GRID_STABLE, the segment-sort queue and scratch).  Returns 0 for invalid

@@ -48,7 +48,7 @@ def test_workspace_bytes(L):
     # look-back words, per-cell counters.  Then scratch: per-CTA chunk sums (up
     # to 4096 CTAs), bucket bases, per-particle slots and (cell, particle) pairs.
     fixed = 4096 + r256(4 * 8 * 8192)   # the header padded to 4 KB
-    assert L.grid_workspace_bytes(p, 0) == (fixed + r256(tiles * 8) + r256(4 * 128 ** 3) + r256(4096 * 4)
+    assert L.grid_workspace_bytes(p, 0) == (fixed + r256(tiles * 8 * 16) + r256(4 * 128 ** 3) + r256(4096 * 4)
                                             + r256(4 * 8192) + r256(4 * 1_000_000) + r256(8 * 1_000_000))
     stable = L.grid_workspace_bytes(p, L.GRID_STABLE)
     assert stable >= L.grid_workspace_bytes(p, 0) + 4 * 1_000_000

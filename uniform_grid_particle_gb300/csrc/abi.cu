@@ -24,7 +24,7 @@ WsLayout ws_layout(uint64_t n, uint64_t cells, unsigned flags) {
     l.bucket_total = off;
     off = round_up(off + kBucketMaxCount * kBucketLanes * sizeof(uint32_t), 256);
     l.tile_status = off;
-    off = round_up(off + scan_tiles(cells) * sizeof(unsigned long long), 256);
+    off = round_up(off + scan_tiles(cells) * kLookStride * sizeof(unsigned long long), 256);
     l.counts = off;
     off = round_up(off + cells * sizeof(uint32_t), 256);
     l.chunk_sums = off;
@@ -179,7 +179,7 @@ int grid_scan(const uint32_t *conteos, uint32_t *inicios, void *ws, const grid_p
     const Span s[] = {{conteos, c * 4}, {inicios, (c + 1) * 4}, {ws, l.total}};
     if (!disjoint(s, 3)) return GRID_EINVAL;
     return cuda_code(launch_scan(const_cast<uint32_t *>(conteos), inicios, c, false, header(ws),
-                                 tile_status(ws, l), static_cast<cudaStream_t>(stream), true));
+                                 tile_status(ws, l), kLookStride, static_cast<cudaStream_t>(stream), true));
 }
 
 int grid_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cursor,
@@ -273,7 +273,7 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
     // dependent launch: each may start while the previous one drains.
     if (e == cudaSuccess) e = launch_count(origen, conteos, celdaDe, p->conteo, g, st, false);  // a2
     if (e == cudaSuccess)  // a3 and a1' (conteos zeroed tile by tile for reuse as the cursor)
-        e = launch_scan(conteos, inicios, c, true, h, tile_status(ws, l), st, true);
+        e = launch_scan(conteos, inicios, c, true, h, tile_status(ws, l), kLookStride, st, true);
     if (e == cudaSuccess)  // a4
         e = launch_scatter(celdaDe, inicios, conteos, ordenado, p->conteo, p->celdas, &h->status,
                            st, true);

@@ -12,7 +12,9 @@
 //
 // Look-back words are 64-bit: flag in the high half (0 = not yet published,
 // 1 = tile total only, 2 = inclusive prefix), value in the low half, written
-// and read with single relaxed gpu-scope accesses.  One warp looks back over
+// and read with single relaxed gpu-scope accesses, `stride` words apart (in a
+// workspace one per 128-byte line: every tile polls every earlier tile's
+// word, and on a few dense lines those polls queued for microseconds).  One warp looks back over
 // 256 predecessors per round (8 words per lane), so while all tiles of a
 // 2M-cell grid are in flight a single round reaches tile 0; only that warp
 // polls, and only the words closer than the nearest inclusive prefix are
@@ -66,7 +68,7 @@ __device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v) {
 // ones are added to it.  Only the words closer than that prefix have to be
 // published; pending ones are re-read together, one round trip per poll,
 // with no sleep between polls (a sleep there cost microseconds).
-__device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t tile,
+__device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t stride, uint32_t tile,
                               uint32_t *status_word) {
     const uint32_t lane = lane_id();
     uint32_t exclusive = 0;
@@ -77,7 +79,7 @@ __device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t ti
 #pragma unroll
         for (int w = 0; w < kLookWords; ++w) {
             const long long idx = j - (long long)(w * 32 + lane);
-            s[w] = idx >= 0 ? load_relaxed(tile_status + idx) : kFlagPrefix;
+            s[w] = idx >= 0 ? load_relaxed(tile_status + (uint64_t)idx * stride) : kFlagPrefix;
         }
         uint32_t nearest;
         while (true) {
@@ -102,7 +104,7 @@ __device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t ti
 #pragma unroll
             for (int w = 0; w < kLookWords; ++w)
                 if ((uint32_t)(w * 32) + lane < nearest && (s[w] >> 32) == 0)
-                    s[w] = load_relaxed(tile_status + (j - (long long)(w * 32 + lane)));
+                    s[w] = load_relaxed(tile_status + (uint64_t)(j - (long long)(w * 32 + lane)) * stride);
         }
         uint32_t sum = 0;
 #pragma unroll
@@ -121,7 +123,7 @@ __device__ uint32_t look_back(const unsigned long long *tile_status, uint32_t ti
 template <bool kZeroInput>
 __global__ void __launch_bounds__(kScanThreads, 2)
 scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, uint32_t tiles,
-            grid_ws_header *hdr, unsigned long long *tile_status) {
+            grid_ws_header *hdr, unsigned long long *tile_status, uint32_t stride) {
     __shared__ uint32_t s_tile;
     __shared__ uint32_t s_warp[kRows][kWarps];
     __shared__ uint32_t s_row[kRows];
@@ -184,10 +186,11 @@ scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, u
             if (tile == 0) {
                 if (lane == 0) store_relaxed(tile_status, kFlagPrefix | tile_total);
             } else {
-                if (lane == 0) store_relaxed(tile_status + tile, kFlagAggregate | tile_total);
-                exclusive = look_back(tile_status, tile, &hdr->status);
+                if (lane == 0) store_relaxed(tile_status + (uint64_t)tile * stride, kFlagAggregate | tile_total);
+                exclusive = look_back(tile_status, stride, tile, &hdr->status);
                 if (lane == 0)
-                    store_relaxed(tile_status + tile, kFlagPrefix | (uint32_t)(exclusive + tile_total));
+                    store_relaxed(tile_status + (uint64_t)tile * stride,
+                                  kFlagPrefix | (uint32_t)(exclusive + tile_total));
             }
             if (lane == 0) s_prefix = exclusive;
         }
@@ -229,7 +232,7 @@ scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, u
     __syncthreads();
     if (s_last) {
         __threadfence();
-        for (uint32_t t = tid; t < tiles; t += kScanThreads) tile_status[t] = 0ull;
+        for (uint32_t t = tid; t < tiles; t += kScanThreads) tile_status[(uint64_t)t * stride] = 0ull;
         if (tid == 0) {
             hdr->scan_ticket = 0u;
             hdr->scan_done = 0u;
@@ -240,14 +243,14 @@ scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, u
 }  // namespace
 
 cudaError_t launch_scan(uint32_t *conteos, uint32_t *inicios, uint64_t cells, bool zero_input,
-                        grid_ws_header *hdr, unsigned long long *tile_status, cudaStream_t s,
+                        grid_ws_header *hdr, unsigned long long *tile_status, uint32_t stride, cudaStream_t s,
                         bool pdl) {
     const uint32_t tiles = (uint32_t)scan_tiles(cells);
     if (zero_input)
         return launch(scan_kernel<true>, tiles, kScanThreads, 0, s, pdl, conteos, inicios, cells,
-                      tiles, hdr, tile_status);
+                      tiles, hdr, tile_status, stride);
     return launch(scan_kernel<false>, tiles, kScanThreads, 0, s, pdl, conteos, inicios, cells,
-                  tiles, hdr, tile_status);
+                  tiles, hdr, tile_status, stride);
 }
 
 }  // namespace ugrid

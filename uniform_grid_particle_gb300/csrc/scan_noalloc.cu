@@ -95,7 +95,7 @@ extern "C" int grid_scan_noalloc(const uint32_t *conteos, uint32_t *inicios, con
     auto *hdr = static_cast<grid_ws_header *>(scratch);
     auto *words =
         reinterpret_cast<unsigned long long *>(static_cast<char *>(scratch) + ugrid::kHeaderBytes);
-    return ugrid::launch_scan(const_cast<uint32_t *>(conteos), inicios, cells, false, hdr, words, s,
+    return ugrid::launch_scan(const_cast<uint32_t *>(conteos), inicios, cells, false, hdr, words, 1u, s,
                               false) == cudaSuccess
                ? GRID_OK
                : GRID_ECUDA;

@@ -40,6 +40,10 @@ constexpr int kScanItems = 16;  // four 16-byte vectors per thread
 constexpr uint32_t kScanTile = kScanThreads * kScanItems;  // 8192 cells
 
 inline uint64_t scan_tiles(uint64_t cells) { return (cells + kScanTile - 1) / kScanTile; }
+// u64 words from one tile's look-back word to the next in a workspace: one
+// 128-byte line each, so that the polls of all tiles spread over many L2
+// slices instead of hammering the few lines a dense array would take.
+constexpr uint32_t kLookStride = 16;
 
 // ---- workspace layout ---------------------------------------------------
 constexpr size_t kHeaderBytes = 256;
@@ -78,7 +82,7 @@ inline BucketPlan bucket_plan(uint64_t n, uint64_t cells, uint32_t ctas) {
 }
 
 struct WsLayout {
-    size_t tile_status;     // u64[tiles]
+    size_t tile_status;     // u64[tiles * kLookStride]: one look-back word per 128-byte line
     size_t chunk_sums;      // u32[kFusedMaxCtas] per-CTA cell-chunk totals (fused build)
     size_t slots;           // u32[n] slot of each particle in its cell (fused build)
     size_t counts;          // u32[cells] counters of the fused build, zero between builds
@@ -119,7 +123,7 @@ cudaError_t launch_count(const ugrid_particula *parts, uint32_t *conteos, uint32
 // inicios = exclusive scan of conteos (C+1 entries).  When zero_input is
 // true the kernel also writes zeros over each conteos tile after reading it.
 cudaError_t launch_scan(uint32_t *conteos, uint32_t *inicios, uint64_t cells, bool zero_input,
-                        grid_ws_header *hdr, unsigned long long *tile_status, cudaStream_t s,
+                        grid_ws_header *hdr, unsigned long long *tile_status, uint32_t stride, cudaStream_t s,
                         bool pdl);
 
 cudaError_t launch_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uint32_t *cursor,
