@@ -45,10 +45,49 @@ __device__ __forceinline__ void sort_in_registers(uint32_t *seg, uint32_t len) {
         if ((uint32_t)k < len) seg[k] = r[k];
 }
 
+__device__ __forceinline__ void compare_exchange(uint32_t &a, uint32_t &b) {
+    const uint32_t lo = min(a, b), hi = max(a, b);
+    a = lo;
+    b = hi;
+}
+
 // Sorts seg[0..len) in the calling thread when len <= kRegisterMax; returns
-// false (nothing done) for longer segments.
+// false (nothing done) for longer segments.  Two to four elements, the common
+// lengths at a few particles per cell, take their optimal networks (1, 3 and
+// 5 compare-exchanges); longer ones a bitonic network of 8, 16 or 32.
 __device__ __forceinline__ bool sort_short_segment(uint32_t *seg, uint32_t len) {
     if (len <= 1) return true;
+    if (len <= 4) {
+        uint32_t a = seg[0], b = seg[1];
+        if (len == 2) {
+            if (a > b) {
+                seg[0] = b;
+                seg[1] = a;
+            }
+            return true;
+        }
+        uint32_t c = seg[2];
+        if (len == 3) {
+            compare_exchange(a, b);
+            compare_exchange(b, c);
+            compare_exchange(a, b);
+            seg[0] = a;
+            seg[1] = b;
+            seg[2] = c;
+            return true;
+        }
+        uint32_t d = seg[3];
+        compare_exchange(a, b);
+        compare_exchange(c, d);
+        compare_exchange(a, c);
+        compare_exchange(b, d);
+        compare_exchange(b, c);
+        seg[0] = a;
+        seg[1] = b;
+        seg[2] = c;
+        seg[3] = d;
+        return true;
+    }
     if (len <= 8)
         sort_in_registers<8>(seg, len);
     else if (len <= 16)
