@@ -264,6 +264,10 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
     __shared__ uint32_t s_own_base[kOwnMax], s_own_count[kOwnMax];
     __shared__ __align__(8) unsigned long long s_gbar[kWarps];  // one per warp, phase D's gather
     __shared__ uint32_t s_long[kLongMax];  // stable mode: cells of the bucket with more than 32 particles
+    // Stable mode: cells of the bucket with two particles or more (the only
+    // segments to sort), listed by the particle that takes slot 1.
+    __shared__ uint32_t s_multi[kStable ? kBucketCap / 2 : 1];
+    __shared__ uint32_t s_nmulti;
     const uint32_t tid = threadIdx.x;
     const uint32_t ctas = gridDim.x;
     const uint32_t B = bk.buckets;
@@ -499,6 +503,7 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
             const uint32_t w = (uint32_t)min((uint64_t)bk.width, a.cells - cl);
             if (tid == 0) {
                 s_nlong = 0u;
+                s_nmulti = 0u;
                 if (B <= 4u * kThreads && j < kOwnMax) {
                     s_base = s_own_base[j];
                     s_count = s_own_count[j];
@@ -529,6 +534,10 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
                 }
                 const uint32_t slot = smem_take(s_table, valid, valid ? local : 0u);
                 if (q < t) s_place[q] = valid ? (local << 16) | slot : 0xffffffffu;
+                if (kStable && valid && slot == 1u) {
+                    const uint32_t m = atomicAdd(&s_nmulti, 1u);
+                    if (m < kBucketCap / 2) s_multi[m] = local;
+                }
             }
             __syncthreads();
             {
@@ -574,8 +583,11 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
                 // Every cell's segment of the bucket sorted by particle index
                 // ("Construir el índice…", §El orden dentro de la celda):
                 // short ones by one thread in registers, the rest by the whole
-                // CTA, one at a time, in shared memory.
-                for (uint32_t l = tid; l < w; l += kThreads) {
+                // CTA, one at a time, in shared memory.  Only the cells of two
+                // particles or more are visited.
+                const uint32_t nmulti = min(s_nmulti, kBucketCap / 2);
+                for (uint32_t i = tid; i < nmulti; i += kThreads) {
+                    const uint32_t l = s_multi[i];
                     const uint32_t s0 = s_table[l] - base, e0 = (l + 1 < w ? s_table[l + 1] : base + t) - base;
                     if (e0 > s0 + 1 && e0 <= t && !sort_short_segment(s_order + s0, e0 - s0)) {
                         const uint32_t q = atomicAdd(&s_nlong, 1u);
