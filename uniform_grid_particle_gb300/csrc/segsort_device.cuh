@@ -203,11 +203,14 @@ __device__ void radix_global(uint32_t *seg, uint32_t *tmp, uint32_t len, uint32_
 
 // Sorts one long segment seg[0..len) with a whole CTA: in shared memory
 // (bitonic) when it fits in `smem_words` (a power of two, at least
-// radix_smem_words<THREADS>()), otherwise by radix through `tmp`.
+// radix_smem_words<THREADS>()), otherwise by radix through `tmp`.  The bitonic
+// path needs the next power of two >= len words of smem.
 template <int THREADS>
 __device__ void sort_long_segment(uint32_t *seg, uint32_t *tmp, uint32_t len, uint32_t n,
                                   uint32_t *smem, uint32_t smem_words) {
-    if (len <= smem_words) {
+    uint32_t padded = 1;  // the bitonic sort fills up to the next power of two
+    while (padded < len) padded <<= 1;
+    if (padded <= smem_words) {
         for (uint32_t i = threadIdx.x; i < len; i += THREADS) smem[i] = seg[i];
         bitonic_shared<THREADS>(smem, len);
         for (uint32_t i = threadIdx.x; i < len; i += THREADS) seg[i] = smem[i];
