@@ -206,13 +206,41 @@ __device__ __forceinline__ void gather_bucket(const CUtensorMap *map, const Buil
         if (lane == 0) mbar_arrive_expect(bar, lanes * 4u * (uint32_t)sizeof(ugrid_particula));
         __syncwarp();
         if (v > 0) gather4_records(smem_addr(stage + 4u * lane * sizeof(ugrid_particula)), map, row, bar);
-        if (!mbar_wait(bar, uses & 1u)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar, uses & 1u))) {  // the warp agrees on a timeout
             if (lane == 0) record_status(status, kStatusTimeout);
             return;
         }
         ++uses;
         if (lane == 0) bulk_store_wait_read(dst, smem_addr(stage), rows * (uint32_t)sizeof(ugrid_particula));
         __syncwarp();
+    }
+}
+
+// Phase C's pairs when phase A could not keep the CTA's cells and ranks
+// (more particles per CTA than its cache holds): cells re-read from celdaDe,
+// places taken from the shared cursors.  Out of line: on the common sizes it
+// never runs, and its code stays out of the way of the code that does.
+__device__ __noinline__ void pairs_from_celdaDe(const BuildArgs a, const BucketScratch bk, uint32_t *s_table,
+                                                uint64_t p_lo, uint64_t p_hi, uint32_t *status) {
+    for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
+        uint32_t cell[kScatterItems];
+#pragma unroll
+        for (int k = 0; k < kScatterItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + threadIdx.x;
+            if (i < p_hi) cell[k] = a.celdaDe[i];
+        }
+#pragma unroll
+        for (int k = 0; k < kScatterItems; ++k) {
+            const uint64_t i = r0 + (uint64_t)k * kThreads + threadIdx.x;
+            const bool valid = i < p_hi;
+            const uint32_t q = smem_take(s_table, valid, valid ? bucket_of(cell[k], bk) : 0u);
+            if (valid) {
+                if (q < a.n)
+                    bk.pairs[q] = make_uint2(cell[k], (uint32_t)i);
+                else
+                    record_status(status, kStatusBounds);
+            }
+        }
     }
 }
 
@@ -276,7 +304,8 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
         s_clean = *reinterpret_cast<volatile uint32_t *>(&hdr->counts_clean) >= a.cells;
         s_bclean = *reinterpret_cast<volatile uint32_t *>(&hdr->buckets_clean) != 0u;
     }
-    for (uint32_t b = tid; b < kBucketMaxCount; b += kThreads) s_table[b] = 0u;
+#pragma unroll
+    for (int q = 0; q < kScanVecs; ++q) s_held[q][tid] = make_uint4(0u, 0u, 0u, 0u);  // s_table, 8192 words
     if ((tid & 31u) == 0) mbar_init(smem_addr(&s_gbar[tid >> 5]));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     uint32_t gather_uses = 0;  // phases of this warp's gather mbarrier
@@ -469,25 +498,8 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
                 else
                     record_status(&hdr->status, kStatusBounds);
             }
-        } else for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
-            uint32_t cell[kScatterItems];
-#pragma unroll
-            for (int k = 0; k < kScatterItems; ++k) {
-                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-                if (i < p_hi) cell[k] = a.celdaDe[i];
-            }
-#pragma unroll
-            for (int k = 0; k < kScatterItems; ++k) {
-                const uint64_t i = r0 + (uint64_t)k * kThreads + tid;
-                const bool valid = i < p_hi;
-                const uint32_t q = smem_take(s_table, valid, valid ? bucket_of(cell[k], bk) : 0u);
-                if (valid) {
-                    if (q < a.n)
-                        bk.pairs[q] = make_uint2(cell[k], (uint32_t)i);
-                    else
-                        record_status(&hdr->status, kStatusBounds);
-                }
-            }
+        } else {
+            pairs_from_celdaDe(a, bk, s_table, p_lo, p_hi, &hdr->status);
         }
         UGRID_PHASE_END(3);
         grid_arrive(hdr, passed);

@@ -93,12 +93,12 @@ reorder_kernel(const __grid_constant__ CUtensorMap origen_map, const uint32_t *_
     for (uint32_t i = 0; i < min(mine, (uint32_t)kStages); ++i) issue(i);
     for (uint32_t i = 0; i < mine; ++i) {
         const uint32_t s = i % kStages;
-        if (!mbar_wait(smem_addr(bar + s), (i / kStages) & 1u)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(bar + s), (i / kStages) & 1u))) {  // the warp agrees
             if (lane == 0) record_status(status, kStatusTimeout);
             // Let the other chunk in flight land (again with a limit) before
             // the CTA leaves.
             for (uint32_t j = i + 1; j < min(mine, i + kStages); ++j)
-                if (!mbar_wait(smem_addr(bar + j % kStages), (j / kStages) & 1u)) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(bar + j % kStages), (j / kStages) & 1u))) break;
             break;
         }
         const uint64_t k0 = (uint64_t)(first + i * stride) * kChunk;
