@@ -35,13 +35,28 @@
 namespace ugrid {
 namespace {
 
+#ifndef UGRID_DENSITY_TILE_CELLS
+#define UGRID_DENSITY_TILE_CELLS 16
+#endif
+#ifndef UGRID_DENSITY_TILE_THREADS
+#define UGRID_DENSITY_TILE_THREADS 320
+#endif
+#ifndef UGRID_DENSITY_STAGE_MAX
+#define UGRID_DENSITY_STAGE_MAX 3584
+#endif
+#ifndef UGRID_DENSITY_SUMS
+#define UGRID_DENSITY_SUMS 4
+#endif
+
 constexpr int kThreads = 256;
-constexpr uint32_t kTileCells = 16;   // cells of one row per CTA (linear order)
-constexpr uint32_t kStageMax = 3584;  // candidates a CTA keeps in shared memory (56 KB: four CTAs per SM)
+constexpr uint32_t kTileCells = UGRID_DENSITY_TILE_CELLS;  // cells of one row per CTA (linear order)
+// Candidates a CTA keeps in shared memory (56 KB: four CTAs per SM).
+constexpr uint32_t kStageMax = UGRID_DENSITY_STAGE_MAX;
 constexpr uint32_t kRowCells = kTileCells + 2;
 // Threads of a tile CTA: one round over its ~kTileCells * 20 own particles at
 // the density of an SPH scene (a second round for a few threads at most).
-constexpr int kTileThreads = 320;
+constexpr int kTileThreads = UGRID_DENSITY_TILE_THREADS;
+constexpr int kSums = UGRID_DENSITY_SUMS;  // running sums: candidates in flight per thread
 
 // sum + masa * max(h^2 - r^2, 0)^3, with h^2 - r^2 taken as three fused
 // multiply-adds from h^2 and the product folded into the last add.
@@ -162,13 +177,14 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
     const uint32_t tid = threadIdx.x;
 
     // Row r = (dz + 1) * 3 + (dy + 1): the cells' starts, relative to the row.
-    for (uint32_t r = tid >> 5, lane = tid & 31u; r < 9; r += kTileThreads / 32) {
+    for (uint32_t idx = tid; idx < 9u * (nc + 1); idx += kTileThreads) {
+        const uint32_t r = idx / (nc + 1), c = idx - r * (nc + 1);
         const int64_t yy = (int64_t)y + (int64_t)(r % 3) - 1, zz = (int64_t)z + (int64_t)(r / 3) - 1;
         const bool exists = yy >= 0 && yy < (int64_t)Y && zz >= 0 && zz < (int64_t)Z;
         const uint64_t row = exists ? (uint64_t)X * ((uint64_t)yy + (uint64_t)Y * (uint64_t)zz) : 0;
         const uint32_t first = exists ? __ldg(inicios + row + xa) : 0u;
-        if (lane <= nc) s_start[r][lane] = exists ? __ldg(inicios + row + xa + lane) - first : 0u;
-        if (lane == 0) s_first[r] = first;
+        s_start[r][c] = exists ? __ldg(inicios + row + xa + c) - first : 0u;
+        if (c == 0) s_first[r] = first;
     }
     __syncthreads();
     if (tid == 0) {
@@ -223,23 +239,30 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
             continue;
         }
         const uint32_t lo = (cx > 0 ? cx - 1 : 0u) - xa, hi = (cx + 1 < X ? cx + 1 : cx) - xa;
-        // Four running sums, so that four candidates are in flight at once;
+        // kSums running sums, so that kSums candidates are in flight at once;
         // both paths add the same terms in the same order.
-        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+        float sum[kSums];
+#pragma unroll
+        for (int u = 0; u < kSums; ++u) sum[u] = 0.0f;
 #pragma unroll 1
         for (int r = 0; r < 9; ++r) {
             const uint32_t a = s_start[r][lo], b = s_start[r][hi + 1];
             uint32_t j = a;
-            for (; j + 4 <= b; j += 4) {
-                const float4 q0 = s_stage[j], q1 = s_stage[j + 1], q2 = s_stage[j + 2], q3 = s_stage[j + 3];
-                s0 = add_term(s0, q0, me.x, me.y, me.z, h2);
-                s1 = add_term(s1, q1, me.x, me.y, me.z, h2);
-                s2 = add_term(s2, q2, me.x, me.y, me.z, h2);
-                s3 = add_term(s3, q3, me.x, me.y, me.z, h2);
+            for (; j + kSums <= b; j += kSums) {
+                float4 q[kSums];
+#pragma unroll
+                for (int u = 0; u < kSums; ++u) q[u] = s_stage[j + u];
+#pragma unroll
+                for (int u = 0; u < kSums; ++u) sum[u] = add_term(sum[u], q[u], me.x, me.y, me.z, h2);
             }
-            for (; j < b; ++j) s0 = add_term(s0, s_stage[j], me.x, me.y, me.z, h2);
+            for (; j < b; ++j) sum[0] = add_term(sum[0], s_stage[j], me.x, me.y, me.z, h2);
         }
-        rho[k] = (s0 + s1) + (s2 + s3);
+        // pairwise: (s0 + s1) + (s2 + s3) for four sums
+#pragma unroll
+        for (int width = kSums / 2; width >= 1; width /= 2)
+#pragma unroll
+            for (int u = 0; u < width; ++u) sum[u] = sum[2 * u] + sum[2 * u + 1];
+        rho[k] = sum[0];
     }
 }
 
