@@ -266,6 +266,135 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
     }
 }
 
+
+// Morton order: one CTA per aligned block of up to 4 x 4 x 4 cells.  The
+// Z-curve lays out each axis's two lowest bits first, so such a block is a
+// run of consecutive codes, and its particles a run of the cell order.  The
+// candidates are the cells of the block widened by one cell on every side,
+// each its own range of the cell order: the CTA copies them to shared memory
+// (a box of up to 6 x 6 x 6 cells, x fastest), then every particle walks its
+// 27 cells there, in the order of the global walk.
+constexpr uint32_t kBoxMax = 6 * 6 * 6;
+constexpr uint32_t kMortonStageMax = 4608;  // candidates kept (72 KB: three CTAs per SM)
+constexpr int kMortonThreads = 320;
+
+__host__ __device__ __forceinline__ uint32_t morton_block_side(uint32_t dim) { return dim < 4u ? dim : 4u; }
+
+template <bool kIndirect>
+__global__ void __launch_bounds__(kMortonThreads)
+density_morton_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
+                           const uint32_t *__restrict__ inicios, Geometry g, float h2, uint32_t n,
+                           float *__restrict__ rho, uint32_t *status) {
+    extern __shared__ float4 s_stage[];          // kMortonStageMax candidates
+    __shared__ uint32_t s_box[kBoxMax + 1];      // stage offset of each box cell, and the end
+    __shared__ uint32_t s_first[kBoxMax];        // cell-order index of each box cell's first particle
+    __shared__ uint32_t s_total;
+    allow_dependent_launch();
+    grid_dependency_wait();
+    const uint32_t X = g.dims[0], Y = g.dims[1], Z = g.dims[2];
+    const uint32_t sx = morton_block_side(X), sy = morton_block_side(Y), sz = morton_block_side(Z);
+    const uint32_t blocks_x = X / sx, blocks_y = Y / sy;
+    const uint32_t bx = blockIdx.x % blocks_x, byz = blockIdx.x / blocks_x;
+    const uint32_t x0 = bx * sx, y0 = (byz % blocks_y) * sy, z0 = (byz / blocks_y) * sz;
+    const uint32_t xa = x0 > 0 ? x0 - 1 : 0u, ya = y0 > 0 ? y0 - 1 : 0u, za = z0 > 0 ? z0 - 1 : 0u;
+    const uint32_t nx = min(x0 + sx, X - 1) - xa + 1, ny = min(y0 + sy, Y - 1) - ya + 1;
+    const uint32_t nz = min(z0 + sz, Z - 1) - za + 1;
+    const uint32_t ncell = nx * ny * nz;
+    const uint32_t tid = threadIdx.x;
+    for (uint32_t i = tid; i < ncell; i += kMortonThreads) {
+        const uint32_t ix = i % nx, iy = (i / nx) % ny, iz = i / (nx * ny);
+        const uint32_t c = cell_at(xa + ix, ya + iy, za + iz, g);
+        const uint32_t f = __ldg(inicios + c), e = __ldg(inicios + c + 1);
+        s_first[i] = f;
+        s_box[i] = e >= f ? e - f : 0xffffffffu;  // starts that decrease send the block to the walk
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t sum = 0;
+        bool fits = true;
+        for (uint32_t i = 0; i < ncell; ++i) {
+            const uint32_t size = s_box[i];
+            if (size > kMortonStageMax || sum + size > kMortonStageMax) fits = false;
+            s_box[i] = sum;
+            sum += fits ? size : 0u;
+        }
+        s_box[ncell] = sum;
+        s_total = fits ? sum : 0xffffffffu;
+    }
+    __syncthreads();
+    const uint32_t total = s_total;
+    const uint32_t c0 = cell_at(x0, y0, z0, g);
+    const uint32_t k0 = __ldg(inicios + c0), k1 = min(__ldg(inicios + c0 + sx * sy * sz), n);
+    if (total == 0xffffffffu) {
+        for (uint32_t k = k0 + tid; k < k1; k += kMortonThreads)
+            density_at<kIndirect, true>(parts, ordenado, inicios, g, h2, n, k, rho, status);
+        return;
+    }
+    // Stage: staged index i belongs to the last box cell whose offset is <= i.
+    for (uint32_t i = tid; i < total; i += kMortonThreads) {
+        uint32_t lo = 0, hi = ncell;  // s_box[lo] <= i < s_box[hi]
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (s_box[mid] <= i)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const uint32_t j = s_first[lo] + (i - s_box[lo]);
+        bool bad = j >= n;
+        const float4 q = bad ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : candidate<kIndirect>(parts, ordenado, j, n, bad);
+        if (bad) record_status(status, kStatusBounds);
+        s_stage[i] = q;
+    }
+    __syncthreads();
+    for (uint32_t k = k0 + tid; k < k1; k += kMortonThreads) {
+        bool bad = false;
+        const float4 me = candidate<kIndirect>(parts, ordenado, k, n, bad);
+        if (bad) {
+            record_status(status, kStatusBounds);
+            continue;
+        }
+        const uint32_t cx = axis_coord(me.x, g.origin[0], g.inv_cell, X);
+        const uint32_t cy = axis_coord(me.y, g.origin[1], g.inv_cell, Y);
+        const uint32_t cz = axis_coord(me.z, g.origin[2], g.inv_cell, Z);
+        if (cx < x0 || cx >= x0 + sx || cy < y0 || cy >= y0 + sy || cz < z0 || cz >= z0 + sz) {
+            density_at<kIndirect, true>(parts, ordenado, inicios, g, h2, n, k, rho, status);
+            continue;
+        }
+        float sum[kSums];
+#pragma unroll
+        for (int u = 0; u < kSums; ++u) sum[u] = 0.0f;
+#pragma unroll 1
+        for (int dz = -1; dz <= 1; ++dz) {
+            const int64_t zz = (int64_t)cz + dz;
+            if (zz < 0 || zz >= (int64_t)Z) continue;
+            for (int dy = -1; dy <= 1; ++dy) {
+                const int64_t yy = (int64_t)cy + dy;
+                if (yy < 0 || yy >= (int64_t)Y) continue;
+                const uint32_t row = nx * (((uint32_t)yy - ya) + ny * ((uint32_t)zz - za));
+                const uint32_t xl = (cx > 0 ? cx - 1 : 0u) - xa, xh = (cx + 1 < X ? cx + 1 : cx) - xa;
+                for (uint32_t ix = xl; ix <= xh; ++ix) {
+                    const uint32_t a = s_box[row + ix], b = s_box[row + ix + 1];
+                    uint32_t j = a;
+                    for (; j + kSums <= b; j += kSums) {
+                        float4 q[kSums];
+#pragma unroll
+                        for (int u = 0; u < kSums; ++u) q[u] = s_stage[j + u];
+#pragma unroll
+                        for (int u = 0; u < kSums; ++u) sum[u] = add_term(sum[u], q[u], me.x, me.y, me.z, h2);
+                    }
+                    for (; j < b; ++j) sum[0] = add_term(sum[0], s_stage[j], me.x, me.y, me.z, h2);
+                }
+            }
+        }
+#pragma unroll
+        for (int width = kSums / 2; width >= 1; width /= 2)
+#pragma unroll
+            for (int u = 0; u < width; ++u) sum[u] = sum[2 * u] + sum[2 * u + 1];
+        rho[k] = sum[0];
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_density(const ugrid_particula *parts, const uint32_t *ordenado,
@@ -286,6 +415,21 @@ cudaError_t launch_density(const ugrid_particula *parts, const uint32_t *ordenad
                                      ordenado, inicios, g, h2, n, rho, status)
                             : launch(density_tile_kernel<false>, (unsigned)tiles, kTileThreads, smem, s, true, p4,
                                      ordenado, inicios, g, h2, n, rho, status);
+        }
+    }
+    if (morton) {
+        const uint64_t blocks = (uint64_t)(g.dims[0] / morton_block_side(g.dims[0])) *
+                                (g.dims[1] / morton_block_side(g.dims[1])) * (g.dims[2] / morton_block_side(g.dims[2]));
+        const size_t smem = kMortonStageMax * sizeof(float4);
+        if (blocks <= 0x7fffffffull) {
+            cudaError_t e = cudaFuncSetAttribute(
+                ordenado ? density_morton_tile_kernel<true> : density_morton_tile_kernel<false>,
+                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            return ordenado ? launch(density_morton_tile_kernel<true>, (unsigned)blocks, kMortonThreads, smem, s, true,
+                                     p4, ordenado, inicios, g, h2, n, rho, status)
+                            : launch(density_morton_tile_kernel<false>, (unsigned)blocks, kMortonThreads, smem, s, true,
+                                     p4, ordenado, inicios, g, h2, n, rho, status);
         }
     }
     const unsigned blocks = (unsigned)((n + kThreads - 1) / kThreads);
