@@ -12,13 +12,15 @@
 // kIndirect = false reads parts (= destino) at j directly; kIndirect = true
 // reads parts (= origen) at ordenado[j].  Both give the same rho[k].
 //
-// Linear order: one CTA per run of kTileCells cells of one (y, z) row.  The
-// candidates of all its particles are the particles of 9 rows of cells
-// (dy, dz in -1..1) over the run widened by one cell at each end, and in
-// linear order each of those is one contiguous range of the cell order.  The
-// CTA copies them to shared memory as (x, y, z, masa) once, then every thread
-// walks its particle's 27 cells there: three consecutive cells per row, nine
-// ranges.  A run whose candidates do not fit falls back to the walk below.
+// Linear order: one CTA per run of kTileCells cells in each of kTileRows
+// consecutive y rows of one z plane (8 x 3 cells).  The candidates of all its
+// particles are the particles of 3 x (kTileRows + 2) rows of cells (the own
+// rows and the rows around them) over the run widened by one cell at each
+// end, and in linear order each of those is one contiguous range of the cell
+// order.  The CTA copies them to shared memory as (x, y, z, masa) once, then
+// every thread walks its particle's 27 cells there: three consecutive cells
+// per row, nine ranges, two candidates at a time.  A run whose candidates do
+// not fit falls back to the walk below.
 //
 // Morton order, and the fallback: one thread per particle walks its 27 cells
 // in global memory.  In Morton order each cell of a row has its own code;
@@ -28,35 +30,42 @@
 // Arithmetic in fp32.  A term is masa * t^3 with t = max(h^2 - r^2, 0), which
 // is the term for r^2 < h^2 and an exact zero otherwise (h^2 - r^2 is formed
 // by fused multiply-adds, so a candidate within an ulp or two of h can fall
-// either way, at a weight of order (ulp of h^2)^3).  Both paths add the same
-// terms in the same order.
+// either way, at a weight of order (ulp of h^2)^3).  On the reordered records
+// and through ordenado a kernel adds the same terms in the same order.
 #include "ugrid_internal.cuh"
 
 namespace ugrid {
 namespace {
 
 #ifndef UGRID_DENSITY_TILE_CELLS
-#define UGRID_DENSITY_TILE_CELLS 16
+#define UGRID_DENSITY_TILE_CELLS 8
 #endif
 #ifndef UGRID_DENSITY_TILE_THREADS
-#define UGRID_DENSITY_TILE_THREADS 320
+#define UGRID_DENSITY_TILE_THREADS 480
 #endif
 #ifndef UGRID_DENSITY_STAGE_MAX
-#define UGRID_DENSITY_STAGE_MAX 3584
+#define UGRID_DENSITY_STAGE_MAX 3328
 #endif
-#ifndef UGRID_DENSITY_SUMS
-#define UGRID_DENSITY_SUMS 4
+#ifndef UGRID_DENSITY_TILE_MIN_BLOCKS
+#define UGRID_DENSITY_TILE_MIN_BLOCKS 4
+#endif
+#ifndef UGRID_DENSITY_TILE_ROWS
+#define UGRID_DENSITY_TILE_ROWS 3
 #endif
 
 constexpr int kThreads = 256;
 constexpr uint32_t kTileCells = UGRID_DENSITY_TILE_CELLS;  // cells of one row per CTA (linear order)
-// Candidates a CTA keeps in shared memory (56 KB: four CTAs per SM).
+// Candidates a CTA keeps in shared memory (52 KB: four CTAs per SM; an SPH
+// scene of 20 particles per cell stages ~3000).
 constexpr uint32_t kStageMax = UGRID_DENSITY_STAGE_MAX;
 constexpr uint32_t kRowCells = kTileCells + 2;
-// Threads of a tile CTA: one round over its ~kTileCells * 20 own particles at
-// the density of an SPH scene (a second round for a few threads at most).
+// Threads of a tile CTA: one round over its ~kTileCells * kTileRows * 20 own
+// particles at the density of an SPH scene (a second round for a few threads
+// at most); four CTAs per SM hold 60 warps.
 constexpr int kTileThreads = UGRID_DENSITY_TILE_THREADS;
-constexpr int kSums = UGRID_DENSITY_SUMS;  // running sums: candidates in flight per thread
+constexpr uint32_t kTileRows = UGRID_DENSITY_TILE_ROWS;  // y rows of cells per CTA
+constexpr uint32_t kStagedRows = 3 * (kTileRows + 2);    // (z, y) rows whose cells are staged
+static_assert(kStageMax % 2 == 0, "the linear tile stages candidates in pairs");
 
 // sum + masa * max(h^2 - r^2, 0)^3, with h^2 - r^2 taken as three fused
 // multiply-adds from h^2 and the product folded into the last add.
@@ -65,6 +74,69 @@ __device__ __forceinline__ float add_term(float sum, float4 q, float px, float p
     const float u = fmaf(-ez, ez, fmaf(-ey, ey, fmaf(-ex, ex, h2)));
     const float t = fmaxf(u, 0.0f);
     return fmaf(q.w * t * t, t, sum);
+}
+
+// The shared-memory tiles keep their candidates in pairs: candidates 2i and
+// 2i + 1 as (x0, x1, y0, y1) and (z0, z1, w0, w1), so that one thread takes
+// two candidates at a time with the packed two-lane fp32 instructions of
+// sm_100 and later.  Both lanes run the arithmetic of add_term with every
+// intermediate negated, which is exact under round-to-nearest: with
+// v = r^2 - h^2 (= -u, the fused multiply-adds taken from -h^2) and
+// m = min(v, 0) = -t, the pair adds masa * m * m * m to a running sum that is
+// the negative of add_term's, and the product masa * m * m equals masa * t * t.
+__device__ __forceinline__ void stage_put(float4 *st, uint32_t j, float4 q) {
+    float *f = reinterpret_cast<float *>(st) + 8u * (j >> 1) + (j & 1u);
+    f[0] = q.x;
+    f[2] = q.y;
+    f[4] = q.z;
+    f[6] = q.w;
+}
+
+__device__ __forceinline__ float4 stage_get(const float4 *st, uint32_t j) {
+    const float *f = reinterpret_cast<const float *>(st) + 8u * (j >> 1) + (j & 1u);
+    return make_float4(f[0], f[2], f[4], f[6]);
+}
+
+// neg - masa * max(h^2 - r^2, 0)^3 for one candidate, as add_term's negative.
+__device__ __forceinline__ float sub_term(float neg, float4 q, float px, float py, float pz, float nh2) {
+    const float ex = q.x - px, ey = q.y - py, ez = q.z - pz;
+    const float m = fminf(fmaf(ez, ez, fmaf(ey, ey, fmaf(ex, ex, nh2))), 0.0f);
+    return fmaf(q.w * m * m, m, neg);
+}
+
+// Both lanes of neg for the candidate pair (a, b) = (x0, x1, y0, y1),
+// (z0, z1, w0, w1); np* = the particle's coordinates negated, in both lanes.
+__device__ __forceinline__ float2 sub_pair(float2 neg, float4 a, float4 b, float2 npx, float2 npy, float2 npz,
+                                           float2 nh2) {
+    const float2 ex = __fadd2_rn(make_float2(a.x, a.y), npx);
+    const float2 ey = __fadd2_rn(make_float2(a.z, a.w), npy);
+    const float2 ez = __fadd2_rn(make_float2(b.x, b.y), npz);
+    float2 v = __ffma2_rn(ex, ex, nh2);
+    v = __ffma2_rn(ey, ey, v);
+    v = __ffma2_rn(ez, ez, v);
+    const float2 m = make_float2(fminf(v.x, 0.0f), fminf(v.y, 0.0f));
+    const float2 w = __fmul2_rn(__fmul2_rn(make_float2(b.z, b.w), m), m);
+    return __ffma2_rn(w, m, neg);
+}
+
+// The candidates [a, b) of a paired stage added to the negated sums: an odd
+// first candidate and an odd last one go to n01.x alone, pairs at even
+// positions alternate between n01 and n23 in groups of four, and a last pair
+// goes to n01.
+__device__ __forceinline__ void walk_range(const float4 *st, uint32_t a, uint32_t b, float4 me, float2 npx,
+                                           float2 npy, float2 npz, float2 nh2v, float2 &n01, float2 &n23) {
+    uint32_t j = a;
+    if ((j & 1u) && j < b) n01.x = sub_term(n01.x, stage_get(st, j++), me.x, me.y, me.z, nh2v.x);
+    for (; j + 4 <= b; j += 4) {
+        const float4 a0 = st[j], b0 = st[j + 1], a1 = st[j + 2], b1 = st[j + 3];
+        n01 = sub_pair(n01, a0, b0, npx, npy, npz, nh2v);
+        n23 = sub_pair(n23, a1, b1, npx, npy, npz, nh2v);
+    }
+    if (j + 2 <= b) {
+        n01 = sub_pair(n01, st[j], st[j + 1], npx, npy, npz, nh2v);
+        j += 2;
+    }
+    if (j < b) n01.x = sub_term(n01.x, stage_get(st, j), me.x, me.y, me.z, nh2v.x);
 }
 
 // (x, y, z, masa) of the particle at cell-order position j.
@@ -157,29 +229,32 @@ density_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ord
 
 // Linear order, one CTA per run of kTileCells cells of one row (see above).
 template <bool kIndirect>
-__global__ void __launch_bounds__(kTileThreads)
+__global__ void __launch_bounds__(kTileThreads, UGRID_DENSITY_TILE_MIN_BLOCKS)
 density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
                     const uint32_t *__restrict__ inicios, Geometry g, float h2, uint32_t n,
                     float *__restrict__ rho, uint32_t *status) {
-    extern __shared__ float4 s_stage[];                 // kStageMax candidates
-    __shared__ uint32_t s_start[9][kRowCells + 1];      // stage offset of each cell of each row, and the end
-    __shared__ uint32_t s_first[9];                     // cell-order index of each row's first candidate
+    extern __shared__ float4 s_stage[];                          // kStageMax candidates
+    __shared__ uint32_t s_start[kStagedRows][kRowCells + 1];     // stage offset of each cell of each row, and the end
+    __shared__ uint32_t s_first[kStagedRows];                    // cell-order index of each row's first candidate
     __shared__ uint32_t s_total;
     allow_dependent_launch();
     grid_dependency_wait();
     const uint32_t X = g.dims[0], Y = g.dims[1], Z = g.dims[2];
-    const uint32_t tiles_x = (X + kTileCells - 1) / kTileCells;
-    const uint32_t tx = blockIdx.x % tiles_x, yz = blockIdx.x / tiles_x;
-    const uint32_t y = yz % Y, z = yz / Y;
+    const uint32_t tiles_x = (X + kTileCells - 1) / kTileCells, tiles_y = (Y + kTileRows - 1) / kTileRows;
+    const uint32_t tx = blockIdx.x % tiles_x, tyz = blockIdx.x / tiles_x;
+    const uint32_t y0 = (tyz % tiles_y) * kTileRows, z = tyz / tiles_y;
+    const uint32_t rows = min(kTileRows, Y - y0);                        // own rows y0 .. y0 + rows - 1
     const uint32_t x0 = tx * kTileCells, x1 = min(x0 + kTileCells, X);  // own cells [x0, x1)
     const uint32_t xa = x0 > 0 ? x0 - 1 : 0u, xb = x1 < X ? x1 : X - 1;  // staged cells [xa, xb]
     const uint32_t nc = xb - xa + 1;
     const uint32_t tid = threadIdx.x;
-
-    // Row r = (dz + 1) * 3 + (dy + 1): the cells' starts, relative to the row.
-    for (uint32_t idx = tid; idx < 9u * (nc + 1); idx += kTileThreads) {
+    // Staged row r = dzi * (kTileRows + 2) + dyi holds the cells [xa, xb] of
+    // row (y0 - 1 + dyi, z - 1 + dzi), if it exists: the cells' starts,
+    // relative to the row.
+    for (uint32_t idx = tid; idx < kStagedRows * (nc + 1); idx += kTileThreads) {
         const uint32_t r = idx / (nc + 1), c = idx - r * (nc + 1);
-        const int64_t yy = (int64_t)y + (int64_t)(r % 3) - 1, zz = (int64_t)z + (int64_t)(r / 3) - 1;
+        const int64_t yy = (int64_t)y0 - 1 + (int64_t)(r % (kTileRows + 2));
+        const int64_t zz = (int64_t)z - 1 + (int64_t)(r / (kTileRows + 2));
         const bool exists = yy >= 0 && yy < (int64_t)Y && zz >= 0 && zz < (int64_t)Z;
         const uint64_t row = exists ? (uint64_t)X * ((uint64_t)yy + (uint64_t)Y * (uint64_t)zz) : 0;
         const uint32_t first = exists ? __ldg(inicios + row + xa) : 0u;
@@ -190,7 +265,7 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
     if (tid == 0) {
         uint32_t base = 0;
         bool fits = true;
-        for (int r = 0; r < 9; ++r) {
+        for (uint32_t r = 0; r < kStagedRows; ++r) {
             const uint32_t size = s_start[r][nc];
             // starts that decrease (inconsistent input) go to the walk, too
             for (uint32_t c = 1; c <= nc; ++c) fits &= s_start[r][c] >= s_start[r][c - 1];
@@ -204,65 +279,70 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
     const uint32_t total = s_total;
     if (total == 0xffffffffu) {
         // The candidates do not fit: each own particle walks global memory.
-        const uint64_t row = (uint64_t)X * ((uint64_t)y + (uint64_t)Y * (uint64_t)z);
-        const uint32_t k0 = __ldg(inicios + row + x0), k1 = min(__ldg(inicios + row + x1), n);
-        for (uint32_t k = k0 + tid; k < k1; k += kTileThreads)
-            density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, k, rho, status);
+        for (uint32_t t = 0; t < rows; ++t) {
+            const uint64_t row = (uint64_t)X * ((uint64_t)(y0 + t) + (uint64_t)Y * (uint64_t)z);
+            const uint32_t k0 = __ldg(inicios + row + x0), k1 = min(__ldg(inicios + row + x1), n);
+            for (uint32_t k = k0 + tid; k < k1; k += kTileThreads)
+                density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, k, rho, status);
+        }
         return;
     }
     // Stage the candidates, row by row.
-    for (int r = 0; r < 9; ++r) {
+    for (uint32_t r = 0; r < kStagedRows; ++r) {
         const uint32_t base = s_start[r][0], size = s_start[r][nc] - base, first = s_first[r];
         for (uint32_t j = tid; j < size; j += kTileThreads) {
             bool bad = first + j >= n;
             const float4 q = bad ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
                                  : candidate<kIndirect>(parts, ordenado, first + j, n, bad);
             if (bad) record_status(status, kStatusBounds);
-            s_stage[base + j] = q;
+            stage_put(s_stage, base + j, q);
         }
     }
     __syncthreads();
-    // The own particles: cells [x0, x1) of the centre row (r = 4).
-    const uint32_t own0 = s_start[4][x0 - xa], own1 = s_start[4][x1 - xa];
-    const uint32_t k_of_stage = s_first[4] - s_start[4][0];  // cell-order index = stage index + this
-    for (uint32_t s = own0 + tid; s < own1; s += kTileThreads) {
-        const float4 me = s_stage[s];
+    // The own particles: cells [x0, x1) of the own rows (staged rows
+    // (kTileRows + 2) + 1 + t), numbered one after the other.
+    uint32_t own_total = 0;
+    for (uint32_t t = 0; t < rows; ++t) {
+        const uint32_t r = (kTileRows + 2) + 1 + t;
+        own_total += s_start[r][x1 - xa] - s_start[r][x0 - xa];
+    }
+    for (uint32_t o = tid; o < own_total; o += kTileThreads) {
+        uint32_t t = 0, before = 0, r = (kTileRows + 2) + 1;
+        for (; t + 1 < rows; ++t, ++r) {
+            const uint32_t here = s_start[r][x1 - xa] - s_start[r][x0 - xa];
+            if (o < before + here) break;
+            before += here;
+        }
+        const uint32_t s = s_start[r][x0 - xa] + (o - before);
+        const float4 me = stage_get(s_stage, s);
         const uint32_t cx = axis_coord(me.x, g.origin[0], g.inv_cell, X);
         const uint32_t cy = axis_coord(me.y, g.origin[1], g.inv_cell, Y);
         const uint32_t cz = axis_coord(me.z, g.origin[2], g.inv_cell, Z);
-        const uint32_t k = k_of_stage + s;
+        const uint32_t k = s_first[r] + (s - s_start[r][0]);
         if (k >= n) continue;
-        if (cx < x0 || cx >= x1 || cy != y || cz != z) {
+        if (cx < x0 || cx >= x1 || cy != y0 + t || cz != z) {
             // Not the cell it is stored in (starts inconsistent with the
             // positions): the walk in global memory, as for any order.
             density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, k, rho, status);
             continue;
         }
         const uint32_t lo = (cx > 0 ? cx - 1 : 0u) - xa, hi = (cx + 1 < X ? cx + 1 : cx) - xa;
-        // kSums running sums, so that kSums candidates are in flight at once;
-        // both paths add the same terms in the same order.
-        float sum[kSums];
-#pragma unroll
-        for (int u = 0; u < kSums; ++u) sum[u] = 0.0f;
+        // Four negated running sums, two candidate pairs in flight.
+        const float2 npx = make_float2(-me.x, -me.x), npy = make_float2(-me.y, -me.y);
+        const float2 npz = make_float2(-me.z, -me.z), nh2v = make_float2(-h2, -h2);
+        float2 n01 = make_float2(-0.0f, -0.0f), n23 = make_float2(-0.0f, -0.0f);
 #pragma unroll 1
-        for (int r = 0; r < 9; ++r) {
-            const uint32_t a = s_start[r][lo], b = s_start[r][hi + 1];
-            uint32_t j = a;
-            for (; j + kSums <= b; j += kSums) {
-                float4 q[kSums];
-#pragma unroll
-                for (int u = 0; u < kSums; ++u) q[u] = s_stage[j + u];
-#pragma unroll
-                for (int u = 0; u < kSums; ++u) sum[u] = add_term(sum[u], q[u], me.x, me.y, me.z, h2);
+        for (int dz = -1; dz <= 1; ++dz) {
+            for (int dy = -1; dy <= 1; ++dy) {
+                const int64_t yy = (int64_t)cy + dy, zz = (int64_t)cz + dz;
+                if (yy < 0 || yy >= (int64_t)Y || zz < 0 || zz >= (int64_t)Z) continue;
+                const uint32_t rr = (uint32_t)(dz + 1) * (kTileRows + 2) + (t + 1 + dy);
+                const uint32_t a = s_start[rr][lo], b = s_start[rr][hi + 1];
+                walk_range(s_stage, a, b, me, npx, npy, npz, nh2v, n01, n23);
             }
-            for (; j < b; ++j) sum[0] = add_term(sum[0], s_stage[j], me.x, me.y, me.z, h2);
         }
-        // pairwise: (s0 + s1) + (s2 + s3) for four sums
-#pragma unroll
-        for (int width = kSums / 2; width >= 1; width /= 2)
-#pragma unroll
-            for (int u = 0; u < width; ++u) sum[u] = sum[2 * u] + sum[2 * u + 1];
-        rho[k] = sum[0];
+        // pairwise, and the sign back: -((s0 + s1) + (s2 + s3))
+        rho[k] = -((n01.x + n01.y) + (n23.x + n23.y));
     }
 }
 
@@ -272,16 +352,23 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
 // run of consecutive codes, and its particles a run of the cell order.  The
 // candidates are the cells of the block widened by one cell on every side,
 // each its own range of the cell order: the CTA copies them to shared memory
-// (a box of up to 6 x 6 x 6 cells, x fastest), then every particle walks its
-// 27 cells there, in the order of the global walk.
+// (a box of up to 6 x 6 x 6 cells, x fastest, in candidate pairs), then every
+// particle walks its 27 cells there as nine ranges, one per row.
 constexpr uint32_t kBoxMax = 6 * 6 * 6;
+#ifndef UGRID_DENSITY_MORTON_THREADS
+#define UGRID_DENSITY_MORTON_THREADS 512
+#endif
+#ifndef UGRID_DENSITY_MORTON_MIN_BLOCKS
+#define UGRID_DENSITY_MORTON_MIN_BLOCKS 3
+#endif
 constexpr uint32_t kMortonStageMax = 4608;  // candidates kept (72 KB: three CTAs per SM)
-constexpr int kMortonThreads = 320;
+constexpr int kMortonThreads = UGRID_DENSITY_MORTON_THREADS;
+static_assert(kMortonStageMax % 2 == 0, "the Morton tile stages candidates in pairs");
 
 __host__ __device__ __forceinline__ uint32_t morton_block_side(uint32_t dim) { return dim < 4u ? dim : 4u; }
 
 template <bool kIndirect>
-__global__ void __launch_bounds__(kMortonThreads)
+__global__ void __launch_bounds__(kMortonThreads, UGRID_DENSITY_MORTON_MIN_BLOCKS)
 density_morton_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
                            const uint32_t *__restrict__ inicios, Geometry g, float h2, uint32_t n,
                            float *__restrict__ rho, uint32_t *status) {
@@ -344,7 +431,7 @@ density_morton_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__re
         bool bad = j >= n;
         const float4 q = bad ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : candidate<kIndirect>(parts, ordenado, j, n, bad);
         if (bad) record_status(status, kStatusBounds);
-        s_stage[i] = q;
+        stage_put(s_stage, i, q);
     }
     __syncthreads();
     for (uint32_t k = k0 + tid; k < k1; k += kMortonThreads) {
@@ -361,9 +448,12 @@ density_morton_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__re
             density_at<kIndirect, true>(parts, ordenado, inicios, g, h2, n, k, rho, status);
             continue;
         }
-        float sum[kSums];
-#pragma unroll
-        for (int u = 0; u < kSums; ++u) sum[u] = 0.0f;
+        // Four negated running sums, two candidate pairs in flight.  The box
+        // keeps x fastest, so the three cells of a row are one stage range.
+        const float2 npx = make_float2(-me.x, -me.x), npy = make_float2(-me.y, -me.y);
+        const float2 npz = make_float2(-me.z, -me.z), nh2v = make_float2(-h2, -h2);
+        float2 n01 = make_float2(-0.0f, -0.0f), n23 = make_float2(-0.0f, -0.0f);
+        const uint32_t xl = (cx > 0 ? cx - 1 : 0u) - xa, xh = (cx + 1 < X ? cx + 1 : cx) - xa;
 #pragma unroll 1
         for (int dz = -1; dz <= 1; ++dz) {
             const int64_t zz = (int64_t)cz + dz;
@@ -372,26 +462,10 @@ density_morton_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__re
                 const int64_t yy = (int64_t)cy + dy;
                 if (yy < 0 || yy >= (int64_t)Y) continue;
                 const uint32_t row = nx * (((uint32_t)yy - ya) + ny * ((uint32_t)zz - za));
-                const uint32_t xl = (cx > 0 ? cx - 1 : 0u) - xa, xh = (cx + 1 < X ? cx + 1 : cx) - xa;
-                for (uint32_t ix = xl; ix <= xh; ++ix) {
-                    const uint32_t a = s_box[row + ix], b = s_box[row + ix + 1];
-                    uint32_t j = a;
-                    for (; j + kSums <= b; j += kSums) {
-                        float4 q[kSums];
-#pragma unroll
-                        for (int u = 0; u < kSums; ++u) q[u] = s_stage[j + u];
-#pragma unroll
-                        for (int u = 0; u < kSums; ++u) sum[u] = add_term(sum[u], q[u], me.x, me.y, me.z, h2);
-                    }
-                    for (; j < b; ++j) sum[0] = add_term(sum[0], s_stage[j], me.x, me.y, me.z, h2);
-                }
+                walk_range(s_stage, s_box[row + xl], s_box[row + xh + 1], me, npx, npy, npz, nh2v, n01, n23);
             }
         }
-#pragma unroll
-        for (int width = kSums / 2; width >= 1; width /= 2)
-#pragma unroll
-            for (int u = 0; u < width; ++u) sum[u] = sum[2 * u] + sum[2 * u + 1];
-        rho[k] = sum[0];
+        rho[k] = -((n01.x + n01.y) + (n23.x + n23.y));
     }
 }
 
@@ -405,7 +479,8 @@ cudaError_t launch_density(const ugrid_particula *parts, const uint32_t *ordenad
     const uint4 *p4 = reinterpret_cast<const uint4 *>(parts);
     const bool morton = g.order != kOrderLinear;
     if (!morton) {
-        const uint64_t tiles = (uint64_t)((g.dims[0] + kTileCells - 1) / kTileCells) * g.dims[1] * g.dims[2];
+        const uint64_t tiles = (uint64_t)((g.dims[0] + kTileCells - 1) / kTileCells) *
+                               ((g.dims[1] + kTileRows - 1) / kTileRows) * g.dims[2];
         const size_t smem = kStageMax * sizeof(float4);
         if (tiles <= 0x7fffffffull) {
             cudaError_t e = cudaFuncSetAttribute(ordenado ? density_tile_kernel<true> : density_tile_kernel<false>,
