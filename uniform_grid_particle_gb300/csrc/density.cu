@@ -18,9 +18,10 @@
 // rows and the rows around them) over the run widened by one cell at each
 // end, and in linear order each of those is one contiguous range of the cell
 // order.  The CTA copies them to shared memory as (x, y, z, masa) once, then
-// every thread walks its particle's 27 cells there: three consecutive cells
-// per row, nine ranges, two candidates at a time.  A run whose candidates do
-// not fit falls back to the walk below.
+// every thread walks the 27 cells of two particles of one cell there: three
+// consecutive cells per row, nine ranges, each candidate load serving both
+// particles and two candidates tested per instruction.  A run whose
+// candidates do not fit falls back to the walk below.
 //
 // Morton order, and the fallback: one thread per particle walks its 27 cells
 // in global memory.  In Morton order each cell of a row has its own code;
@@ -41,7 +42,7 @@ namespace {
 #define UGRID_DENSITY_TILE_CELLS 8
 #endif
 #ifndef UGRID_DENSITY_TILE_THREADS
-#define UGRID_DENSITY_TILE_THREADS 480
+#define UGRID_DENSITY_TILE_THREADS 288
 #endif
 #ifndef UGRID_DENSITY_STAGE_MAX
 #define UGRID_DENSITY_STAGE_MAX 3328
@@ -59,9 +60,9 @@ constexpr uint32_t kTileCells = UGRID_DENSITY_TILE_CELLS;  // cells of one row p
 // scene of 20 particles per cell stages ~3000).
 constexpr uint32_t kStageMax = UGRID_DENSITY_STAGE_MAX;
 constexpr uint32_t kRowCells = kTileCells + 2;
-// Threads of a tile CTA: one round over its ~kTileCells * kTileRows * 20 own
-// particles at the density of an SPH scene (a second round for a few threads
-// at most); four CTAs per SM hold 60 warps.
+// Threads of a tile CTA: one round over its work items, two particles each,
+// ~kTileCells * kTileRows * 10 at the density of an SPH scene (a second round
+// for a few threads at most); four CTAs per SM.
 constexpr int kTileThreads = UGRID_DENSITY_TILE_THREADS;
 constexpr uint32_t kTileRows = UGRID_DENSITY_TILE_ROWS;  // y rows of cells per CTA
 constexpr uint32_t kStagedRows = 3 * (kTileRows + 2);    // (z, y) rows whose cells are staged
@@ -137,6 +138,42 @@ __device__ __forceinline__ void walk_range(const float4 *st, uint32_t a, uint32_
         j += 2;
     }
     if (j < b) n01.x = sub_term(n01.x, stage_get(st, j), me.x, me.y, me.z, nh2v.x);
+}
+
+// walk_range for two particles A and B of one cell at once: each stage load
+// serves both, and each particle's sums take the same terms in the same order
+// as walk_range gives them.
+struct PairSums {
+    float2 n01, n23;
+};
+__device__ __forceinline__ void walk_range2(const float4 *st, uint32_t a, uint32_t b, float4 ma, float4 mb,
+                                            float2 nh2v, PairSums &sa, PairSums &sb) {
+    const float2 ax = make_float2(-ma.x, -ma.x), ay = make_float2(-ma.y, -ma.y), az = make_float2(-ma.z, -ma.z);
+    const float2 bx = make_float2(-mb.x, -mb.x), by = make_float2(-mb.y, -mb.y), bz = make_float2(-mb.z, -mb.z);
+    uint32_t j = a;
+    if ((j & 1u) && j < b) {
+        const float4 q = stage_get(st, j++);
+        sa.n01.x = sub_term(sa.n01.x, q, ma.x, ma.y, ma.z, nh2v.x);
+        sb.n01.x = sub_term(sb.n01.x, q, mb.x, mb.y, mb.z, nh2v.x);
+    }
+    for (; j + 4 <= b; j += 4) {
+        const float4 a0 = st[j], b0 = st[j + 1], a1 = st[j + 2], b1 = st[j + 3];
+        sa.n01 = sub_pair(sa.n01, a0, b0, ax, ay, az, nh2v);
+        sb.n01 = sub_pair(sb.n01, a0, b0, bx, by, bz, nh2v);
+        sa.n23 = sub_pair(sa.n23, a1, b1, ax, ay, az, nh2v);
+        sb.n23 = sub_pair(sb.n23, a1, b1, bx, by, bz, nh2v);
+    }
+    if (j + 2 <= b) {
+        const float4 a0 = st[j], b0 = st[j + 1];
+        sa.n01 = sub_pair(sa.n01, a0, b0, ax, ay, az, nh2v);
+        sb.n01 = sub_pair(sb.n01, a0, b0, bx, by, bz, nh2v);
+        j += 2;
+    }
+    if (j < b) {
+        const float4 q = stage_get(st, j);
+        sa.n01.x = sub_term(sa.n01.x, q, ma.x, ma.y, ma.z, nh2v.x);
+        sb.n01.x = sub_term(sb.n01.x, q, mb.x, mb.y, mb.z, nh2v.x);
+    }
 }
 
 // (x, y, z, masa) of the particle at cell-order position j.
@@ -237,6 +274,7 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
     __shared__ uint32_t s_start[kStagedRows][kRowCells + 1];     // stage offset of each cell of each row, and the end
     __shared__ uint32_t s_first[kStagedRows];                    // cell-order index of each row's first candidate
     __shared__ uint32_t s_total;
+    __shared__ uint32_t s_items[kTileRows * kTileCells + 1];     // first work item of each own cell, and the end
     allow_dependent_launch();
     grid_dependency_wait();
     const uint32_t X = g.dims[0], Y = g.dims[1], Z = g.dims[2];
@@ -274,6 +312,16 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
             base += size;
         }
         s_total = fits ? base : 0xffffffffu;
+        // One work item per two particles of an own cell (an odd last one alone).
+        uint32_t items = 0, q = 0;
+        for (uint32_t t = 0; t < rows; ++t) {
+            const uint32_t r = (kTileRows + 2) + 1 + t;
+            for (uint32_t c = x0 - xa; c < x1 - xa; ++c, ++q) {
+                s_items[q] = items;
+                items += (s_start[r][c + 1] - s_start[r][c] + 1) / 2;
+            }
+        }
+        s_items[q] = items;
     }
     __syncthreads();
     const uint32_t total = s_total;
@@ -299,50 +347,53 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
         }
     }
     __syncthreads();
-    // The own particles: cells [x0, x1) of the own rows (staged rows
-    // (kTileRows + 2) + 1 + t), numbered one after the other.
-    uint32_t own_total = 0;
-    for (uint32_t t = 0; t < rows; ++t) {
-        const uint32_t r = (kTileRows + 2) + 1 + t;
-        own_total += s_start[r][x1 - xa] - s_start[r][x0 - xa];
-    }
-    for (uint32_t o = tid; o < own_total; o += kTileThreads) {
-        uint32_t t = 0, before = 0, r = (kTileRows + 2) + 1;
-        for (; t + 1 < rows; ++t, ++r) {
-            const uint32_t here = s_start[r][x1 - xa] - s_start[r][x0 - xa];
-            if (o < before + here) break;
-            before += here;
+    // Work item o: two particles of one own cell (the last of an odd cell
+    // alone), which share their 27 cells; items run over the own cells row by
+    // row.
+    const uint32_t w = x1 - x0, own_cells = rows * w, items = s_items[own_cells];
+    for (uint32_t o = tid; o < items; o += kTileThreads) {
+        uint32_t lo = 0, hi = own_cells;  // s_items[lo] <= o < s_items[hi]
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (s_items[mid] <= o)
+                lo = mid;
+            else
+                hi = mid;
         }
-        const uint32_t s = s_start[r][x0 - xa] + (o - before);
-        const float4 me = stage_get(s_stage, s);
-        const uint32_t cx = axis_coord(me.x, g.origin[0], g.inv_cell, X);
-        const uint32_t cy = axis_coord(me.y, g.origin[1], g.inv_cell, Y);
-        const uint32_t cz = axis_coord(me.z, g.origin[2], g.inv_cell, Z);
-        const uint32_t k = s_first[r] + (s - s_start[r][0]);
-        if (k >= n) continue;
-        if (cx < x0 || cx >= x1 || cy != y0 + t || cz != z) {
-            // Not the cell it is stored in (starts inconsistent with the
+        const uint32_t t = lo / w, c = (x0 - xa) + (lo - t * w), r = (kTileRows + 2) + 1 + t;
+        const uint32_t s0 = s_start[r][c] + 2u * (o - s_items[lo]);
+        const uint32_t s1 = s0 + 1u < s_start[r][c + 1] ? s0 + 1u : s0;  // s1 == s0: A alone
+        const float4 ma = stage_get(s_stage, s0), mb = stage_get(s_stage, s1);
+        const uint32_t ka = s_first[r] + (s0 - s_start[r][0]), kb = s_first[r] + (s1 - s_start[r][0]);
+        const uint32_t cx = x0 + (c - (x0 - xa)), cy = y0 + t;
+        const bool in_a = axis_coord(ma.x, g.origin[0], g.inv_cell, X) == cx &&
+                          axis_coord(ma.y, g.origin[1], g.inv_cell, Y) == cy &&
+                          axis_coord(ma.z, g.origin[2], g.inv_cell, Z) == z;
+        const bool in_b = axis_coord(mb.x, g.origin[0], g.inv_cell, X) == cx &&
+                          axis_coord(mb.y, g.origin[1], g.inv_cell, Y) == cy &&
+                          axis_coord(mb.z, g.origin[2], g.inv_cell, Z) == z;
+        if (ka >= n || kb >= n) continue;
+        if (!in_a || !in_b) {
+            // Not the cell they are stored in (starts inconsistent with the
             // positions): the walk in global memory, as for any order.
-            density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, k, rho, status);
+            density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, ka, rho, status);
+            if (s1 != s0) density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, kb, rho, status);
             continue;
         }
-        const uint32_t lo = (cx > 0 ? cx - 1 : 0u) - xa, hi = (cx + 1 < X ? cx + 1 : cx) - xa;
-        // Four negated running sums, two candidate pairs in flight.
-        const float2 npx = make_float2(-me.x, -me.x), npy = make_float2(-me.y, -me.y);
-        const float2 npz = make_float2(-me.z, -me.z), nh2v = make_float2(-h2, -h2);
-        float2 n01 = make_float2(-0.0f, -0.0f), n23 = make_float2(-0.0f, -0.0f);
+        const uint32_t lo_c = (cx > 0 ? cx - 1 : 0u) - xa, hi_c = (cx + 1 < X ? cx + 1 : cx) - xa;
+        const float2 nh2v = make_float2(-h2, -h2);
+        PairSums sa{make_float2(-0.0f, -0.0f), make_float2(-0.0f, -0.0f)}, sb = sa;
 #pragma unroll 1
         for (int dz = -1; dz <= 1; ++dz) {
             for (int dy = -1; dy <= 1; ++dy) {
-                const int64_t yy = (int64_t)cy + dy, zz = (int64_t)cz + dz;
+                const int64_t yy = (int64_t)cy + dy, zz = (int64_t)z + dz;
                 if (yy < 0 || yy >= (int64_t)Y || zz < 0 || zz >= (int64_t)Z) continue;
                 const uint32_t rr = (uint32_t)(dz + 1) * (kTileRows + 2) + (t + 1 + dy);
-                const uint32_t a = s_start[rr][lo], b = s_start[rr][hi + 1];
-                walk_range(s_stage, a, b, me, npx, npy, npz, nh2v, n01, n23);
+                walk_range2(s_stage, s_start[rr][lo_c], s_start[rr][hi_c + 1], ma, mb, nh2v, sa, sb);
             }
         }
-        // pairwise, and the sign back: -((s0 + s1) + (s2 + s3))
-        rho[k] = -((n01.x + n01.y) + (n23.x + n23.y));
+        rho[ka] = -((sa.n01.x + sa.n01.y) + (sa.n23.x + sa.n23.y));
+        if (s1 != s0) rho[kb] = -((sb.n01.x + sb.n01.y) + (sb.n23.x + sb.n23.y));
     }
 }
 
