@@ -23,10 +23,14 @@
 // particles and two candidates tested per instruction.  A run whose
 // candidates do not fit falls back to the walk below.
 //
-// Morton order, and the fallback: one thread per particle walks its 27 cells
-// in global memory.  In Morton order each cell of a row has its own code;
-// codes that follow one another (an even x and the x after it) are merged
-// into one range.
+// Morton order: one CTA per aligned block of up to 4 x 4 x 4 cells, its box
+// of neighbour cells staged the same way (see density_morton_tile_kernel).
+//
+// The fallback, for a tile whose candidates do not fit and for a particle not
+// in the cell it is stored in: one thread per particle walks its 27 cells in
+// global memory.  In Morton order each cell of a row has its own code; codes
+// that follow one another (an even x and the x after it) are merged into one
+// range.
 //
 // Arithmetic in fp32.  A term is masa * t^3 with t = max(h^2 - r^2, 0), which
 // is the term for r^2 < h^2 and an exact zero otherwise (h^2 - r^2 is formed
