@@ -313,6 +313,46 @@ def pin_density_brute_force(o, seed: int = 14) -> None:
             assert np.allclose(got, want, rtol=1e-12, atol=1e-300), f"dims {dims} h {h}"
 
 
+def pin_density_stale_grid(o, seed: int = 15) -> None:
+    """A grid built before the particles moved: each particle walks the 27
+    cells around the cell of its current position, and a candidate counts
+    where the grid lists it (its cell at build time), at its current position.
+    Brute force over all pairs with that membership rule."""
+    rng = np.random.default_rng(seed)
+    for order in (0, 1):
+        dims, origin, cs, n = (4, 4, 4), (-1.0, 0.5, 2.0), 0.5, 600
+        lo, hi = np.array(origin), np.array(origin) + np.array(dims) * cs
+        before = np.zeros((n, 8), np.float32)
+        before[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+        before[:, 7] = (0.5 + rng.random(n)).astype(np.float32)
+        after = before.copy()
+        after[:, :3] += (rng.uniform(-0.4, 0.4, (n, 3)) * cs).astype(np.float32)
+        grid = o.build(before, dims, origin, cs, order=order)
+        now = o.build(after, dims, origin, cs, order=order)
+        # cell coordinates from the cell index of each order
+        code_xyz = {}
+        for z in range(dims[2]):
+            for y in range(dims[1]):
+                for x in range(dims[0]):
+                    c = x + dims[0] * (y + dims[1] * z) if order == 0 else o.morton_cell(x, y, z, dims)
+                    code_xyz[c] = np.array((x, y, z))
+        listed = np.array([code_xyz[int(c)] for c in grid["celdaDe"]])
+        current = np.array([code_xyz[int(c)] for c in now["celdaDe"]])
+        moved = int(np.sum(np.any(listed != current, axis=1)))
+        assert moved > n // 4, "the displacement moves a good share of the particles"
+        pos, m = after[:, :3].astype(np.float64), after[:, 7].astype(np.float64)
+        for h in (cs, 0.7 * cs):
+            want = np.zeros(n)
+            for i in range(n):
+                near = np.all(np.abs(listed - current[i]) <= 1, axis=1)
+                e = pos[near] - pos[i]
+                r2 = e[:, 0] * e[:, 0] + e[:, 1] * e[:, 1] + e[:, 2] * e[:, 2]
+                t = np.where(r2 < h * h, h * h - r2, 0.0)
+                want[i] = float(np.sum(m[near] * t * t * t))
+            got = o.density(after, dims, origin, cs, grid["inicios"], grid["ordenado"], h, order=order)
+            assert np.allclose(got, want, rtol=1e-12, atol=1e-300), f"order {order} h {h}"
+
+
 def pin_density_closed_forms(o) -> None:
     dims, origin, cs, h = (8, 8, 8), (0.0, 0.0, 0.0), 1.0, 1.0
     # one particle alone: its own mass times h^6
@@ -472,6 +512,7 @@ ALL_PINS = [
     pin_reorder_records,
     pin_density_closed_forms,
     pin_density_brute_force,
+    pin_density_stale_grid,
     pin_morton_index_table,
     pin_morton_bijection_and_blocks,
     pin_morton_matches_xor_comparator,
