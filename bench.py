@@ -2,7 +2,7 @@
 """Benchmark of the uniform-grid build on GB300; prints one JSON line.
 
 A step is one whole build (count, scan, scatter, gather: grid_build, one
-cooperative launch of the fused build kernel) of the headline scene: 1,000,000 particles uniform in
+cooperative launch of the bucketed build kernel) of the headline scene: 1,000,000 particles uniform in
 [-5, 5)^3 on a 128^3 grid, 32-byte records, inputs resident in HBM.  L2 is
 flushed (a 2 x L2-size buffer is written) between steps, outside the timed
 events.  Per step the build is bracketed by CUDA events on the stream it is

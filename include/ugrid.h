@@ -227,12 +227,16 @@ int grid_build_host(const ugrid_particula *origen_host, ugrid_particula *destino
  *            otherwise GRID_ERANGE is returned and nothing is enqueued.
  * Returns GRID_OK, GRID_EINVAL (bad params or arrays, nothing enqueued),
  * GRID_ERANGE, or GRID_ECUDA.  The first call on each device (with that
- * device current) looks up the array's device address and caches it; make
- * that first call before capturing any stream.  All calls share the one
+ * device current) looks up the array's device address and caches it with the
+ * current context; make that first call before capturing any stream.  After
+ * the device's context is destroyed and created again (cudaDeviceReset), the
+ * next call finds a new context and looks the address up again, so that call
+ * too should come before any capture.  All calls share the one
  * array, which each call clears on its stream before use: calls whose work
  * overlaps on the GPU race on it and must be ordered by the caller.  A
  * device-side wait that gives up is recorded only in that array and is not
- * reported. */
+ * reported: a caller that needs to detect it uses grid_scan with a workspace
+ * and grid_status. */
 int grid_scan_noalloc(const uint32_t *conteos, uint32_t *inicios, const grid_params *p,
                       void *stream);
 

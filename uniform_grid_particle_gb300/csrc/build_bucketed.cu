@@ -321,14 +321,12 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
     // and for the CTA's particles in bucket order.
     const bool grouped = cached && B <= 4u * kThreads && 2u * B + mine <= kBucketMaxCount;
 
-    UGRID_PHASE_MARK(0);
     if (!s_bclean) {
         for (uint32_t b = blockIdx.x * kThreads + tid; b < B; b += ctas * kThreads) zero_bucket(bk.total, b);
         grid_barrier(hdr, passed);
     }
 
     // ---- A: cells and the bucket totals ------------------------------------------
-    UGRID_PHASE_MARK(1);
     {
         unsigned long long keep;
         asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
@@ -365,7 +363,6 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
         if (grouped) s_table[B + b] = m;  // the histogram, kept for phase C
         if (m) s_table[b] = atomicAdd(bk.total + (uint64_t)b * kBucketLanes + blockIdx.x % kBucketLanes, m);
     }
-    UGRID_PHASE_END(1);
     grid_arrive(hdr, passed);
     if (grouped) {
         // Phase C writes this CTA's pairs as runs of consecutive positions,
@@ -404,7 +401,6 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
     if (blockIdx.x == 0 && tid == 0) hdr->buckets_clean = 0u;
 
     // ---- C: bucket bases, this CTA's stretch of each bucket, the pairs ------------
-    UGRID_PHASE_MARK(3);
     bool heavy;
     {
         const uint32_t lane_r = blockIdx.x % kBucketLanes;
@@ -471,7 +467,6 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
     }
     __syncthreads();
 
-    UGRID_PHASE_MARK(2);
     if (heavy) {
         atomic_path<kStable>(a, g, hdr, ws, bk, s_clean != 0u, passed, p_lo, p_hi, s_held, s_red, s_rows);
     } else {
@@ -501,7 +496,6 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
         } else {
             pairs_from_celdaDe(a, bk, s_table, p_lo, p_hi, &hdr->status);
         }
-        UGRID_PHASE_END(3);
         grid_arrive(hdr, passed);
         // The first bucket's cell table is cleared while the barrier fills.
 #pragma unroll
@@ -509,7 +503,6 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
         grid_wait(hdr, passed);
 
         // ---- D: each bucket placed by one CTA ---------------------------------
-        UGRID_PHASE_MARK(4);
         for (uint32_t b = blockIdx.x, j = 0; b < B; b += ctas, ++j) {
             const uint64_t cl = (uint64_t)b * bk.width;
             const uint32_t w = (uint32_t)min((uint64_t)bk.width, a.cells - cl);
@@ -579,7 +572,6 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
                 }
             }
             __syncthreads();
-            UGRID_PHASE_MARK(5);
             for (uint32_t q = tid; q < t; q += kThreads) {
                 const uint32_t place = s_place[q];
                 if (place != 0xffffffffu) {
@@ -620,7 +612,6 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
                     __syncthreads();
                 }
             }
-            UGRID_PHASE_MARK(7);
             for (uint32_t q = tid; q < t; q += kThreads) a.ordenado[base + q] = s_order[q];
             // The bucket's records, gathered in order ("El kernel de
             // reordenación": destino[k] = origen[ordenado[k]]), through
@@ -644,7 +635,6 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
         if (blockIdx.x == 0 && tid == 0) a.inicios[a.cells] = a.n;
     }
     if ((tid & 31u) == 0) bulk_wait_all();
-    UGRID_PHASE_MARK(6);
     // The last CTA out: every bucket word has been zeroed.
     if (tid == 0 && atomicAdd(&hdr->bar_exit, 1u) == ctas - 1u) {
         if ((hdr->status & kStatusTimeout) == 0) hdr->buckets_clean = 1u;

@@ -85,41 +85,32 @@ build_fused_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch ws
     uint64_t p_lo, p_hi;
     particle_range(a.n, p_lo, p_hi);
 
-    UGRID_PHASE_MARK(0);
     // ---- clear the counters, only if the previous build did not leave them zero
     if (!s_clean) {
         clear_counters(ws.counts, a.cells);
         grid_barrier(hdr, passed);
     }
 
-    UGRID_PHASE_MARK(1);
     count_phase<true>(a, g, ws, p_lo, p_hi, s_held);
-    UGRID_PHASE_END(1);
     grid_barrier(hdr, passed);
     // The counters are not zero until the scan has run to the end.
     if (blockIdx.x == 0 && tid == 0) hdr->counts_clean = 0u;
 
-    UGRID_PHASE_MARK(2);
     const ScanChunk chunk = scan_chunk(a.cells);
     scan_totals_phase(ws, chunk, s_held, s_red);
-    UGRID_PHASE_END(2);
     grid_barrier(hdr, passed);
 
-    UGRID_PHASE_MARK(3);
     scan_starts_phase(a, ws, chunk, s_held, s_red, s_rows);
-    UGRID_PHASE_END(3);
     grid_barrier(hdr, passed);
     // Every CTA zeroed its counters before that barrier.
     if (blockIdx.x == 0 && tid == 0 && (hdr->status & kStatusTimeout) == 0)
         hdr->counts_clean = (uint32_t)a.cells;
 
-    UGRID_PHASE_MARK(4);
     if constexpr (!kStable) {
         scatter_move_phase(a, ws, &hdr->status, p_lo, p_hi);
     } else {
         stable_tail_phase(a, ws, hdr, passed, p_lo, p_hi, s_held);
     }
-    UGRID_PHASE_MARK(6);
     leave_launch(hdr);
 }
 

@@ -42,33 +42,19 @@
 namespace ugrid {
 namespace {
 
-#ifndef UGRID_DENSITY_TILE_CELLS
-#define UGRID_DENSITY_TILE_CELLS 8
-#endif
-#ifndef UGRID_DENSITY_TILE_THREADS
-#define UGRID_DENSITY_TILE_THREADS 288
-#endif
-#ifndef UGRID_DENSITY_STAGE_MAX
-#define UGRID_DENSITY_STAGE_MAX 3328
-#endif
-#ifndef UGRID_DENSITY_TILE_MIN_BLOCKS
-#define UGRID_DENSITY_TILE_MIN_BLOCKS 4
-#endif
-#ifndef UGRID_DENSITY_TILE_ROWS
-#define UGRID_DENSITY_TILE_ROWS 3
-#endif
 
 constexpr int kThreads = 256;
-constexpr uint32_t kTileCells = UGRID_DENSITY_TILE_CELLS;  // cells of one row per CTA (linear order)
+constexpr uint32_t kTileCells = 8;  // cells of one row per CTA (linear order)
 // Candidates a CTA keeps in shared memory (52 KB: four CTAs per SM; an SPH
 // scene of 20 particles per cell stages ~3000).
-constexpr uint32_t kStageMax = UGRID_DENSITY_STAGE_MAX;
+constexpr uint32_t kStageMax = 3328;
 constexpr uint32_t kRowCells = kTileCells + 2;
 // Threads of a tile CTA: one round over its work items, two particles each,
 // ~kTileCells * kTileRows * 10 at the density of an SPH scene (a second round
 // for a few threads at most); four CTAs per SM.
-constexpr int kTileThreads = UGRID_DENSITY_TILE_THREADS;
-constexpr uint32_t kTileRows = UGRID_DENSITY_TILE_ROWS;  // y rows of cells per CTA
+constexpr int kTileThreads = 288;
+constexpr int kTileMinBlocks = 4;  // CTAs per SM the tile kernel is compiled for
+constexpr uint32_t kTileRows = 3;  // y rows of cells per CTA
 constexpr uint32_t kStagedRows = 3 * (kTileRows + 2);    // (z, y) rows whose cells are staged
 static_assert(kStageMax % 2 == 0, "the linear tile stages candidates in pairs");
 
@@ -270,7 +256,7 @@ density_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ord
 
 // Linear order, one CTA per run of kTileCells cells of one row (see above).
 template <bool kIndirect>
-__global__ void __launch_bounds__(kTileThreads, UGRID_DENSITY_TILE_MIN_BLOCKS)
+__global__ void __launch_bounds__(kTileThreads, kTileMinBlocks)
 density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
                     const uint32_t *__restrict__ inicios, Geometry g, float h2, uint32_t n,
                     float *__restrict__ rho, uint32_t *status) {
@@ -410,20 +396,15 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
 // (a box of up to 6 x 6 x 6 cells, x fastest, in candidate pairs), then every
 // particle walks its 27 cells there as nine ranges, one per row.
 constexpr uint32_t kBoxMax = 6 * 6 * 6;
-#ifndef UGRID_DENSITY_MORTON_THREADS
-#define UGRID_DENSITY_MORTON_THREADS 512
-#endif
-#ifndef UGRID_DENSITY_MORTON_MIN_BLOCKS
-#define UGRID_DENSITY_MORTON_MIN_BLOCKS 3
-#endif
 constexpr uint32_t kMortonStageMax = 4608;  // candidates kept (72 KB: three CTAs per SM)
-constexpr int kMortonThreads = UGRID_DENSITY_MORTON_THREADS;
+constexpr int kMortonThreads = 512;
+constexpr int kMortonMinBlocks = 3;  // CTAs per SM the Morton tile kernel is compiled for
 static_assert(kMortonStageMax % 2 == 0, "the Morton tile stages candidates in pairs");
 
 __host__ __device__ __forceinline__ uint32_t morton_block_side(uint32_t dim) { return dim < 4u ? dim : 4u; }
 
 template <bool kIndirect>
-__global__ void __launch_bounds__(kMortonThreads, UGRID_DENSITY_MORTON_MIN_BLOCKS)
+__global__ void __launch_bounds__(kMortonThreads, kMortonMinBlocks)
 density_morton_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
                            const uint32_t *__restrict__ inicios, Geometry g, float h2, uint32_t n,
                            float *__restrict__ rho, uint32_t *status) {

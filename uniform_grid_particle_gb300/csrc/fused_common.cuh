@@ -11,34 +11,12 @@
 namespace ugrid {
 namespace fused {
 
-// Measurement hook at each phase boundary; compiled out unless a profiling
-// build defines it.
-#ifndef UGRID_PHASE_MARK
-#define UGRID_PHASE_MARK(phase)
-#endif
-#ifndef UGRID_PHASE_END
-#define UGRID_PHASE_END(phase)
-#endif
-
-#ifndef UGRID_FUSED_COUNT_ITEMS
-#define UGRID_FUSED_COUNT_ITEMS 4
-#endif
-#ifndef UGRID_FUSED_SCATTER_ITEMS
-#define UGRID_FUSED_SCATTER_ITEMS 8
-#endif
-#ifndef UGRID_FUSED_GATHER_ITEMS
-#define UGRID_FUSED_GATHER_ITEMS 4
-#endif
-#ifndef UGRID_FUSED_MOVE_ITEMS
-#define UGRID_FUSED_MOVE_ITEMS 4
-#endif
-
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCountItems = UGRID_FUSED_COUNT_ITEMS;      // particles per thread per round
-constexpr int kScatterItems = UGRID_FUSED_SCATTER_ITEMS;  // particles per thread per round
-constexpr int kGatherItems = UGRID_FUSED_GATHER_ITEMS;    // half-records per thread per round
-constexpr int kMoveItems = UGRID_FUSED_MOVE_ITEMS;        // half-records per thread per round
+constexpr int kCountItems = 4;    // particles per thread per round
+constexpr int kScatterItems = 8;  // particles per thread per round
+constexpr int kGatherItems = 4;   // half-records per thread per round
+constexpr int kMoveItems = 4;     // half-records per thread per round
 constexpr int kScanVecs = 4;  // 16-byte vectors of counts a thread keeps between the scan phases
 constexpr int kAggBits = 11;  // the count's per-CTA grouping table: 2^11 entries
 constexpr int kAggSlots = 1 << kAggBits;

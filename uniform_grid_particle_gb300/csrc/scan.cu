@@ -196,8 +196,13 @@ scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, u
         }
         __syncthreads();
         // This CTA reads no more look-back words: count it out now, so the
-        // last one can clear them while the others still write inicios.
-        if (tid == 0) s_last = atomicAdd(&hdr->scan_done, 1u) == gridDim.x - 1 ? 1u : 0u;
+        // last one can clear them while the others still write inicios.  The
+        // fence orders this CTA's last publish (by this same thread) before
+        // the count-out, so the last CTA's reset cannot be overtaken by it.
+        if (tid == 0) {
+            __threadfence();
+            s_last = atomicAdd(&hdr->scan_done, 1u) == gridDim.x - 1 ? 1u : 0u;
+        }
 
         const uint32_t prefix = s_prefix;
 #pragma unroll
@@ -225,6 +230,7 @@ scan_kernel(uint32_t *conteos, uint32_t *__restrict__ inicios, uint64_t cells, u
         if (tile == tiles - 1 && tid == 0) inicios[cells] = prefix + tile_total;
     } else if (tid == 0) {
         record_status(&hdr->status, kStatusBounds);  // more CTAs than tiles: a stale ticket
+        __threadfence();
         s_last = atomicAdd(&hdr->scan_done, 1u) == gridDim.x - 1 ? 1u : 0u;
     }
 

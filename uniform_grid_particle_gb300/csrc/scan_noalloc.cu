@@ -17,16 +17,19 @@
 //
 // Host code never uses the array's name as a device address (in host code it
 // names a host-side stand-in).  The first call on each device, with that device
-// current, looks the address up with cudaGetSymbolAddress and caches it; make
-// that first call before capturing any stream.  Every call clears the header
+// current, looks the address up with cudaGetSymbolAddress and caches it with
+// the device's current context; make that first call before capturing any
+// stream.  A call that finds another context current (the primary context
+// was reset and created again, so the module and its array were loaded
+// anew) looks the address up again.  Every call clears the header
 // and the look-back words it will use with cudaMemsetAsync on its stream, then
 // launches the same scan kernel as grid_scan.  All calls share the one array:
 // calls whose work overlaps on the GPU (different streams, or different host
 // threads without ordering) race on it and must be serialised by the caller.
 // Device-side diagnostics (a look-back wait that gave up) land in the array's
 // status word and are not reported by this entry point.
-#include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include "ugrid_internal.cuh"
 
@@ -40,21 +43,52 @@ constexpr size_t kNoAllocScratchBytes =
 static __device__ __align__(256) unsigned char g_scan_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void *> g_scratch_address[kMaxDevices];
+
+// The array's address on each device, and the context it was looked up in.
+struct CachedAddress {
+    CUcontext ctx;
+    void *ptr;
+};
+CachedAddress g_scratch_address[kMaxDevices];
+std::mutex g_scratch_mutex;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+// cuCtxGetCurrent from the driver, looked up through the runtime once.
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    return fn;
+}
 
 // Device address of g_scan_scratch on the current device, looked up once per
-// device and cached.
+// device and context and cached.  Before the runtime has made the device's
+// context current the driver reports none; the symbol lookup then creates it.
 cudaError_t scratch_address(void **out) {
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return e;
+    const CtxGetCurrentFn get = ctx_get_current();
+    if (get == nullptr) return cudaErrorDeviceUninitialized;
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
     const bool cacheable = device >= 0 && device < kMaxDevices;
-    void *p = cacheable ? g_scratch_address[device].load(std::memory_order_acquire) : nullptr;
-    if (p == nullptr) {
-        e = cudaGetSymbolAddress(&p, g_scan_scratch);
-        if (e != cudaSuccess) return e;
-        if (cacheable) g_scratch_address[device].store(p, std::memory_order_release);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (cacheable && ctx != nullptr && g_scratch_address[device].ctx == ctx) {
+        *out = g_scratch_address[device].ptr;
+        return cudaSuccess;
     }
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scan_scratch);
+    if (e != cudaSuccess) return e;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+    if (cacheable) g_scratch_address[device] = CachedAddress{ctx, p};
     *out = p;
     return cudaSuccess;
 }
