@@ -13,10 +13,14 @@ Further passes in the same run:
                    per-kernel microseconds and the gather kernel's roofline;
   * end to end   — host buffers: pinned host origen -> device, build,
                    destino and inicios -> pinned host, all inside the events;
-  * neighbours   — the neighbour query on an SPH-like scene (5.2M particles,
-                   64^3 cells, ~84 neighbours), in linear and Morton cell
-                   order, on the reordered records and through ordenado:
+  * neighbours   — the neighbour query on SPH-like scenes (20 and 50
+                   particles per cell on 64^3 cells), in linear and Morton
+                   cell order, on the reordered records and through ordenado:
                    the reorder's gain and the Z-curve's;
+  * workloads    — every workload (tiny, scan-dominated, headline,
+                   contention, stress with its ten ping-pong builds), whole
+                   builds with L2 flushed before each: microseconds,
+                   algorithmic GB/s and the fraction of the HBM peak;
   * cpu baseline — the CPU oracle (single thread) on the same scene.
 
 ``--impl reference`` times the CPU oracle alone (the reference arm).
@@ -303,6 +307,144 @@ def workload_config(scene, args) -> dict:
     }
 
 
+# The five workloads, each timed as whole builds with L2 flushed before every
+# build (the headline is the line's own value; it is timed again here so that
+# every row comes from the same pass).
+CONFIG_SCENES = ["tiny", "scan_dominated", "headline", "contention", "stress"]
+
+
+def time_configs(ug, scenes, flags: int, steps: int, warmup: int, timed, settle, stream, peak: float) -> dict:
+    """Per workload: mean and median microseconds per build, Mparticles/s,
+    algorithmic GB/s and the fraction of the HBM peak.  The stress workload
+    runs its ten ping-pong builds (each reads the previous build's destino)
+    `max(1, steps // 10)` times from the original scene and reports build 1 and
+    builds 2-10 apart."""
+    import statistics
+
+    import torch
+
+    out = {}
+    for name in CONFIG_SCENES:
+        scene = scenes.SCENES[name]
+        rows = scene.particles()
+        n, cells = scene.n, scene.cells
+        alg = sum(algorithmic_bytes(n, cells).values())
+        p = ug.make_params(n, scene.dims, scene.origin, scene.cell_size)
+        origen = torch.from_numpy(rows).cuda()
+        del rows
+        b = ug.GridBuffers.allocate(p, flags)
+
+        def one(src, dst):
+            ug.grid_build(src, dst.destino, dst.conteos, dst.celdaDe, dst.inicios, dst.ordenado, dst.ws, p,
+                          flags, stream)
+
+        def row(us: list[float]) -> dict:
+            mean = statistics.mean(us)
+            gbs = alg / (mean * 1e-6) / 1e9
+            return {"us_mean": mean, "us_median": statistics.median(us), "mparticles_per_s": n / mean,
+                    "achieved_gbs": gbs, "frac": gbs / peak, "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+
+        entry = {"n": n, "cells": cells, "algorithmic_bytes": alg}
+        if scene.builds > 1:
+            pong = ug.GridBuffers.allocate(p, flags)
+            first, rest = [], []
+            for k in range(warmup):
+                settle(k)
+                one(origen, b)
+            for rep in range(max(1, steps // scene.builds)):
+                src, bufs = origen, [b, pong]
+                for k in range(scene.builds):
+                    dst = bufs[k % 2]
+                    ms = timed(lambda: one(src, dst), 1)[0]
+                    (first if k == 0 else rest).append(1e3 * ms)
+                    src = dst.destino
+            for bufs_ in (b, pong):
+                if ug.grid_status(bufs_.ws) != 0:
+                    raise RuntimeError(f"device status set during the {name} builds")
+            entry["build1"] = row(first)
+            entry["builds_2_on"] = row(rest)
+            entry["steps"] = {"build1": len(first), "builds_2_on": len(rest)}
+            del pong
+        else:
+            for k in range(warmup):
+                settle(k)
+                one(origen, b)
+            us = [1e3 * ms for ms in timed(lambda: one(origen, b), steps)]
+            if ug.grid_status(b.ws) != 0:
+                raise RuntimeError(f"device status set during the {name} builds")
+            entry.update(row(us))
+            entry["steps"] = steps
+        out[name] = entry
+        del b, origen
+        torch.cuda.empty_cache()
+    return out
+
+
+def neighbour_query(ug, sph, warmup: int, steps: int, timed, settle, stream) -> dict:
+    """grid_density on one SPH-like scene, in linear and Morton order, on the
+    reordered records and through ordenado, L2 flushed before every step:
+    microseconds, the reorder's gain, the Z-curve's, and the ALU roofline of
+    the linear query on the reordered records."""
+    import statistics
+
+    import numpy as np
+    import torch
+
+    origen_s = torch.from_numpy(sph.particles()).cuda()
+    rho = torch.empty(sph.n, dtype=torch.float32, device="cuda")
+    h = sph.cell_size
+    out = {
+        "scene": f"{sph.name}: N={sph.n:,}, grid {sph.dims[0]}^3, h = cellSize = {h:.6f}",
+        "mean_particles_per_cell": sph.n / sph.cells,
+        "l2": "flushed between steps",
+        "steps": steps,
+    }
+    tests = 0
+    for order_name, order in (("linear", ug.GRID_ORDER_LINEAR), ("morton", ug.GRID_ORDER_MORTON)):
+        ps = ug.make_params(sph.n, sph.dims, sph.origin, sph.cell_size, order=order)
+        bs = ug.GridBuffers.allocate(ps)
+        bs.build(origen_s, ps, stream=stream)
+
+        def q_sorted():
+            ug.grid_density(bs.destino, bs.inicios, rho, bs.ws, ps, h, stream=stream)
+
+        def q_indirect():
+            ug.grid_density(origen_s, bs.inicios, rho, bs.ws, ps, h, ordenado=bs.ordenado, stream=stream)
+
+        for k in range(warmup):
+            settle(k)
+            q_sorted()
+            q_indirect()
+        sorted_ms = statistics.mean(timed(q_sorted, steps))
+        indirect_ms = statistics.mean(timed(q_indirect, steps))
+        if ug.grid_status(bs.ws) != 0:
+            raise RuntimeError(f"device status {ug.grid_status(bs.ws)} after the neighbour query")
+        out[f"us_{order_name}_sorted"] = 1e3 * sorted_ms
+        out[f"us_{order_name}_indirect"] = 1e3 * indirect_ms
+        if order == ug.GRID_ORDER_LINEAR:
+            tests = pair_tests(bs.conteos.cpu().numpy().view(np.uint32), sph.dims)
+        del bs
+    out["reorder_gain"] = out["us_linear_indirect"] / out["us_linear_sorted"]
+    out["morton_gain_sorted"] = out["us_linear_sorted"] / out["us_morton_sorted"]
+    out["morton_gain_indirect"] = out["us_linear_indirect"] / out["us_morton_indirect"]
+    best = min(out[f"us_{o}_sorted"] for o in ("linear", "morton"))
+    out["mparticles_per_s_best"] = sph.n / best
+    # The query does one distance test per (particle, candidate in its 27
+    # cells): 7 fp32 operations (3 differences, 1 product, 2 fused
+    # multiply-adds, 1 comparison).  Its ceiling is the fp32 lanes at the
+    # maximum SM clock: 152 SMs x 128 lanes x 2.07 GHz / 7.
+    tests_per_s = tests / (out["us_linear_sorted"] * 1e-6) / 1e9
+    alu_peak = ALU_LANES * ALU_CLOCK_GHZ / PAIR_TEST_OPS
+    out["roofline"] = {"bound": "alu", "kernel": "density_tile_kernel<0> (linear, reordered records)",
+                       "achieved": tests_per_s, "peak": alu_peak, "unit": "Gpair-tests/s",
+                       "frac": tests_per_s / alu_peak, "pair_tests_per_query": int(tests),
+                       "peak_derivation": f"{ALU_LANES} fp32 lanes x {ALU_CLOCK_GHZ} GHz / "
+                                          f"{PAIR_TEST_OPS} ops per test"}
+    del origen_s, rho
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------- GPU arm
 
 def run_gpu(args) -> None:
@@ -523,59 +665,17 @@ def run_gpu(args) -> None:
     if not np.array_equal(host_inicios.numpy()[[0, cells]], np.array([0, n], dtype=np.int32)):
         raise RuntimeError("end-to-end result is inconsistent")
 
-    # ---- neighbour query on an SPH-like scene: cell order x access path ----
-    neighbour = None
+    # ---- neighbour query on SPH-like scenes: cell order x access path ----
+    neighbour = neighbour_dense = None
     if args.density_steps > 0:
-        sph = scenes.SCENES["sph"]
-        origen_s = torch.from_numpy(sph.particles()).cuda()
-        rho = torch.empty(sph.n, dtype=torch.float32, device="cuda")
-        h = sph.cell_size
-        neighbour = {
-            "scene": f"sph: N={sph.n:,}, grid {sph.dims[0]}^3, h = cellSize = {h:.6f}",
-            "mean_particles_per_cell": sph.n / sph.cells,
-            "l2": "flushed between steps",
-        }
-        for order_name, order in (("linear", ug.GRID_ORDER_LINEAR), ("morton", ug.GRID_ORDER_MORTON)):
-            ps = ug.make_params(sph.n, sph.dims, sph.origin, sph.cell_size, order=order)
-            bs = ug.GridBuffers.allocate(ps)
-            bs.build(origen_s, ps, stream=stream)
+        neighbour = neighbour_query(ug, scenes.SCENES["sph"], args.warmup, args.density_steps, timed, settle, stream)
+        neighbour_dense = neighbour_query(ug, scenes.SCENES["sph_dense"], args.warmup,
+                                          max(3, args.density_steps // 4), timed, settle, stream)
 
-            def q_sorted():
-                ug.grid_density(bs.destino, bs.inicios, rho, bs.ws, ps, h, stream=stream)
-
-            def q_indirect():
-                ug.grid_density(origen_s, bs.inicios, rho, bs.ws, ps, h, ordenado=bs.ordenado, stream=stream)
-
-            for k in range(args.warmup):
-                settle(k)
-                q_sorted()
-                q_indirect()
-            sorted_ms = statistics.mean(timed(q_sorted, args.density_steps))
-            indirect_ms = statistics.mean(timed(q_indirect, args.density_steps))
-            if ug.grid_status(bs.ws) != 0:
-                raise RuntimeError(f"device status {ug.grid_status(bs.ws)} after the neighbour query")
-            neighbour[f"us_{order_name}_sorted"] = 1e3 * sorted_ms
-            neighbour[f"us_{order_name}_indirect"] = 1e3 * indirect_ms
-            if order == ug.GRID_ORDER_LINEAR:
-                tests = pair_tests(bs.conteos.cpu().numpy().view(np.uint32), sph.dims)
-            del bs
-        neighbour["reorder_gain"] = neighbour["us_linear_indirect"] / neighbour["us_linear_sorted"]
-        neighbour["morton_gain_sorted"] = neighbour["us_linear_sorted"] / neighbour["us_morton_sorted"]
-        neighbour["morton_gain_indirect"] = neighbour["us_linear_indirect"] / neighbour["us_morton_indirect"]
-        best = min(neighbour[f"us_{o}_sorted"] for o in ("linear", "morton"))
-        neighbour["mparticles_per_s_best"] = sph.n / best
-        # The query does one distance test per (particle, candidate in its 27
-        # cells): 7 fp32 operations (3 differences, 1 product, 2 fused
-        # multiply-adds, 1 comparison).  Its ceiling is the fp32 lanes at the
-        # maximum SM clock: 152 SMs x 128 lanes x 2.07 GHz / 7.
-        tests_per_s = tests / (neighbour["us_linear_sorted"] * 1e-6) / 1e9
-        alu_peak = ALU_LANES * ALU_CLOCK_GHZ / PAIR_TEST_OPS
-        neighbour["roofline"] = {"bound": "alu", "kernel": "density_tile_kernel<0> (linear, reordered records)",
-                                 "achieved": tests_per_s, "peak": alu_peak, "unit": "Gpair-tests/s",
-                                 "frac": tests_per_s / alu_peak, "pair_tests_per_query": int(tests),
-                                 "peak_derivation": f"{ALU_LANES} fp32 lanes x {ALU_CLOCK_GHZ} GHz / "
-                                                    f"{PAIR_TEST_OPS} ops per test"}
-        del origen_s, rho
+    # ---- every workload, whole builds, L2 flushed before each ----
+    configs = None
+    if args.config_steps > 0:
+        configs = time_configs(ug, scenes, flags, args.config_steps, args.warmup, timed, settle, stream, peak)
 
     if rank != 0:
         if dist is not None:
@@ -613,6 +713,8 @@ def run_gpu(args) -> None:
                 "d2h_bytes_per_step": int(host_dest.numel() * 4 + host_inicios.numel() * 4),
                 "ms_per_step": e2e_total / len(e2e_ms)},
         "neighbour_query": neighbour,
+        "neighbour_query_dense": neighbour_dense,
+        "configs": configs,
         "gpu_launches": kernels_per_step * args.steps,
         "clocks": clocks.summary(),
     }
@@ -632,6 +734,8 @@ def main(argv=None) -> None:
     ap.add_argument("--graph-steps", type=int, default=2000)
     ap.add_argument("--density-steps", type=int, default=20,
                     help="steps of the neighbour-query leg (0 skips it)")
+    ap.add_argument("--config-steps", type=int, default=30,
+                    help="timed builds of each of the five workloads (0 skips that leg)")
     ap.add_argument("--phase-steps", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time")

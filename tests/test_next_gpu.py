@@ -140,3 +140,70 @@ def test_density_empty_scene(ug):
     inicios = torch.zeros(65, dtype=torch.int32, device="cuda")
     ug.grid_density(None, inicios, torch.empty(0, device="cuda"), ws, p, 1.0)
     assert ug.grid_status(ws) == 0
+
+
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("h_frac", [1.0, 0.7])
+def test_density_stale_grid(ug, oracle_lib, order, h_frac):
+    """A grid built before the particles moved ("Construir el índice…", §La
+    dispersión: the query walks the cells the grid lists).  Each particle
+    walks the 27 cells around the cell of its current position, and a
+    candidate counts where the grid lists it, at its current position: the
+    reading the oracle follows (pinned against all pairs with that membership
+    rule).  About 12 particles per cell, so the tiles serve most runs and the
+    moved particles take the per-particle walk."""
+    rng = np.random.default_rng(40 + order)
+    dims, cs = (32, 32, 32), np.float32(0.3125)
+    origin = (np.float32(-5.0), np.float32(-5.0), np.float32(-5.0))
+    n = 12 * dims[0] * dims[1] * dims[2]
+    lo = np.array(origin, np.float64)
+    hi = lo + np.array(dims) * float(cs)
+    before = np.zeros((n, 8), np.float32)
+    before[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+    before[:, 3] = 1.0
+    before[:, 7] = (0.5 + rng.random(n)).astype(np.float32)
+    after = before.copy()
+    moving = rng.random(n) < 0.3
+    after[moving, :3] += (rng.uniform(-0.45, 0.45, (int(moving.sum()), 3)) * cs).astype(np.float32)
+    p = ug.make_params(n, dims, origin, cs, order=order)
+    got = gpu_build(ug, before, dims, origin, cs, params=p)
+    ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
+    inicios = torch.from_numpy(got["inicios"].view(np.int32)).cuda()
+    ordenado = torch.from_numpy(got["ordenado"].view(np.int32)).cuda()
+    h = float(cs) * h_frac
+    rho_sorted = torch.empty(n, dtype=torch.float32, device="cuda")
+    rho_indirect = torch.empty(n, dtype=torch.float32, device="cuda")
+    # the records in the grid's order, at their current positions
+    ug.grid_density(torch.from_numpy(after[got["ordenado"]]).cuda(), inicios, rho_sorted, ws, p, h)
+    ug.grid_density(torch.from_numpy(after).cuda(), inicios, rho_indirect, ws, p, h, ordenado=ordenado)
+    assert ug.grid_status(ws) == 0
+    a, b = rho_sorted.cpu().numpy(), rho_indirect.cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), "both paths add the same terms in the same order"
+    ref = oracle_lib.density(after, dims, origin, cs, got["inicios"], got["ordenado"], h, order=order)
+    by_particle = np.empty(n, np.float64)
+    by_particle[got["ordenado"]] = a
+    scale = float(after[:, 7].max()) * h ** 6
+    err = np.abs(by_particle - ref)
+    assert np.all(err <= 1e-4 * (ref + scale)), f"max error {err.max()} (rho up to {ref.max()})"
+    # the moved particles really left their cells
+    now = oracle_lib.cell_index(after, dims, origin, cs, order=order)
+    assert int(np.sum(now != got["celdaDe"])) > n // 20
+
+
+@pytest.mark.parametrize("order", [0, 1])
+def test_density_dense_cells(ug, oracle_lib, order):
+    """50 particles per cell, near the top of the 20-60 per cell that
+    "Contar partículas por celda" (§La contención) calls healthy, on a grid
+    with power-of-two sides (so it also builds in Morton order)."""
+    rng = np.random.default_rng(50 + order)
+    dims, cs = (32, 32, 16), np.float32(0.25)
+    origin = (np.float32(-4.0), np.float32(-4.0), np.float32(-2.0))
+    n = 50 * dims[0] * dims[1] * dims[2]
+    lo = np.array(origin, np.float64)
+    hi = lo + np.array(dims) * float(cs)
+    rows = np.zeros((n, 8), np.float32)
+    rows[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+    rows[:, 3] = 1.0
+    rows[:, 7] = (0.5 + rng.random(n)).astype(np.float32)
+    ref = _density_case(ug, oracle_lib, rows, dims, origin, cs, cs, order=order)
+    assert float(np.median(ref)) > 0.0

@@ -278,3 +278,39 @@ def test_scan_large_counts(ug, oracle_lib):
         ug.grid_scan(torch.from_numpy(conteos.view(np.int32)).cuda(), inicios, ws, p)
         assert np.array_equal(to_u32(inicios), oracle_lib.exclusive_scan(conteos))
     assert ug.grid_status(ws) == 0
+
+
+# Scenes of a few million particles: more buckets than CTAs, so every CTA
+# places several buckets in phase D, and skewed ones whose crowded buckets
+# take the atomic fallback; at grid sizes that need no more than a few seconds
+# of oracle time.
+LARGE = [
+    ("uniform", 4_194_304, (160, 160, 160)),
+    ("skewed", 2_500_000, (128, 128, 128)),
+    ("one_cell_heavy", 1_500_000, (64, 64, 64)),
+]
+
+
+def _large_rows(kind: str, n: int, dims) -> np.ndarray:
+    if kind == "uniform":
+        rows = scenes.uniform_particles(n, 0xC0FFEE)
+    elif kind == "skewed":
+        rows = scenes.contention_particles(n, 0xC0FFEF, dims[0])
+    else:
+        # a third of the particles on one cell centre, the rest uniform
+        rows = scenes.uniform_particles(n, 0xC0FFF0)
+        centre = np.float32(-5.0 + (dims[0] // 3 + 0.5) * (10.0 / dims[0]))
+        rows[: n // 3, :3] = centre
+    return rows
+
+
+@pytest.mark.parametrize("stable", [False, True], ids=["atomic", "stable"])
+@pytest.mark.parametrize("kind,n,dims", LARGE, ids=[g[0] for g in LARGE])
+def test_large_scenes(ug, oracle_lib, kind, n, dims, stable):
+    rows = _large_rows(kind, n, dims)
+    cs = float(np.float32(10.0 / dims[0]))
+    origin = (-5.0, -5.0, -5.0)
+    ref = oracle_lib.build(rows, dims, origin, cs)
+    flags = ug.GRID_STABLE if stable else 0
+    got = gpu_build(ug, rows, dims, origin, cs, flags=flags)
+    assert_matches_oracle(oracle_lib, rows, got, ref, stable)

@@ -254,6 +254,122 @@ density_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ord
     if (k < n) density_at<kIndirect, kMorton>(parts, ordenado, inicios, g, h2, n, (uint32_t)k, rho, status);
 }
 
+// A tile whose candidates fit in shared memory one z plane at a time only
+// (denser scenes: the pages put a healthy cell at 20 to 60 particles): the
+// three planes are staged one after the other, and every work item keeps its
+// two particles' sums in registers across the planes (up to kSliceRounds work
+// items per thread).  Each plane's three rows give a partial sum in the same
+// way as the whole tile does; the particle's density is the sum of the three
+// partial sums, in plane order.  A particle not in the cell it is stored in
+// takes the walk in global memory.
+constexpr uint32_t kSliceRounds = 3;
+template <bool kIndirect>
+__device__ __forceinline__ void tile_by_planes(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
+                                               const uint32_t *__restrict__ inicios, const Geometry &g, float h2,
+                                               uint32_t n, float *__restrict__ rho, uint32_t *status,
+                                               float4 *s_stage, const uint32_t (*s_start)[kRowCells + 1],
+                                               const uint32_t *s_first, const uint32_t *s_items, uint32_t x0,
+                                               uint32_t x1, uint32_t xa, uint32_t y0, uint32_t z, uint32_t rows) {
+    const uint32_t X = g.dims[0], Y = g.dims[1], Z = g.dims[2];
+    const uint32_t tid = threadIdx.x;
+    const uint32_t w = x1 - x0, own_cells = rows * w, items = s_items[own_cells];
+    const uint32_t nc = (x1 < X ? x1 : X - 1) - xa + 1;
+    const float2 nh2v = make_float2(-h2, -h2);
+    float acc[kSliceRounds][2];
+#pragma unroll
+    for (uint32_t rd = 0; rd < kSliceRounds; ++rd) acc[rd][0] = acc[rd][1] = 0.0f;
+    for (uint32_t p = 0; p < 3; ++p) {
+        const int64_t zz = (int64_t)z - 1 + (int64_t)p;
+        if (zz < 0 || zz >= (int64_t)Z) continue;
+        const uint32_t r0 = p * (kTileRows + 2);
+        const uint32_t pbase = s_start[r0][0];
+        __syncthreads();  // the previous plane's stage has been read
+        for (uint32_t r = r0; r < r0 + kTileRows + 2; ++r) {
+            const uint32_t base = s_start[r][0] - pbase, size = s_start[r][nc] - s_start[r][0], first = s_first[r];
+            for (uint32_t j = tid; j < size; j += kTileThreads) {
+                bool bad = first + j >= n;
+                const float4 q = bad ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
+                                     : candidate<kIndirect>(parts, ordenado, first + j, n, bad);
+                if (bad) record_status(status, kStatusBounds);
+                stage_put(s_stage, base + j, q);
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (uint32_t rd = 0; rd < kSliceRounds; ++rd) {
+            const uint32_t o = tid + rd * kTileThreads;
+            if (o >= items) continue;
+            uint32_t lo = 0, hi = own_cells;  // s_items[lo] <= o < s_items[hi]
+            while (hi - lo > 1) {
+                const uint32_t mid = (lo + hi) >> 1;
+                if (s_items[mid] <= o)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+            const uint32_t t = lo / w, c = (x0 - xa) + (lo - t * w), r = (kTileRows + 2) + 1 + t;
+            const uint32_t s0 = s_start[r][c] + 2u * (o - s_items[lo]);
+            const uint32_t s1 = s0 + 1u < s_start[r][c + 1] ? s0 + 1u : s0;
+            const uint32_t ka = s_first[r] + (s0 - s_start[r][0]), kb = s_first[r] + (s1 - s_start[r][0]);
+            bool bad = false;
+            const float4 ma = candidate<kIndirect>(parts, ordenado, ka, n, bad);
+            const float4 mb = candidate<kIndirect>(parts, ordenado, kb, n, bad);
+            if (bad) continue;
+            const uint32_t cx = x0 + (c - (x0 - xa)), cy = y0 + t;
+            const uint32_t lo_c = (cx > 0 ? cx - 1 : 0u) - xa, hi_c = (cx + 1 < X ? cx + 1 : cx) - xa;
+            PairSums sa{make_float2(-0.0f, -0.0f), make_float2(-0.0f, -0.0f)}, sb = sa;
+#pragma unroll 1
+            for (int dy = -1; dy <= 1; ++dy) {
+                const int64_t yy = (int64_t)cy + dy;
+                if (yy < 0 || yy >= (int64_t)Y) continue;
+                const uint32_t rr = r0 + (t + 1 + dy);
+                walk_range2(s_stage, s_start[rr][lo_c] - pbase, s_start[rr][hi_c + 1] - pbase, ma, mb, nh2v, sa, sb);
+            }
+            acc[rd][0] += -((sa.n01.x + sa.n01.y) + (sa.n23.x + sa.n23.y));
+            acc[rd][1] += -((sb.n01.x + sb.n01.y) + (sb.n23.x + sb.n23.y));
+        }
+    }
+#pragma unroll
+    for (uint32_t rd = 0; rd < kSliceRounds; ++rd) {
+        const uint32_t o = tid + rd * kTileThreads;
+        if (o >= items) continue;
+        uint32_t lo = 0, hi = own_cells;
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (s_items[mid] <= o)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const uint32_t t = lo / w, c = (x0 - xa) + (lo - t * w), r = (kTileRows + 2) + 1 + t;
+        const uint32_t s0 = s_start[r][c] + 2u * (o - s_items[lo]);
+        const uint32_t s1 = s0 + 1u < s_start[r][c + 1] ? s0 + 1u : s0;
+        const uint32_t ka = s_first[r] + (s0 - s_start[r][0]), kb = s_first[r] + (s1 - s_start[r][0]);
+        if (ka >= n || kb >= n) {
+            record_status(status, kStatusBounds);
+            continue;
+        }
+        bool bad = false;
+        const float4 ma = candidate<kIndirect>(parts, ordenado, ka, n, bad);
+        const float4 mb = candidate<kIndirect>(parts, ordenado, kb, n, bad);
+        const uint32_t cx = x0 + (c - (x0 - xa)), cy = y0 + t;
+        const bool in_a = axis_coord(ma.x, g.origin[0], g.inv_cell, X) == cx &&
+                          axis_coord(ma.y, g.origin[1], g.inv_cell, Y) == cy &&
+                          axis_coord(ma.z, g.origin[2], g.inv_cell, Z) == z;
+        const bool in_b = axis_coord(mb.x, g.origin[0], g.inv_cell, X) == cx &&
+                          axis_coord(mb.y, g.origin[1], g.inv_cell, Y) == cy &&
+                          axis_coord(mb.z, g.origin[2], g.inv_cell, Z) == z;
+        if (!in_a || !in_b) {
+            // Not the cell they are stored in: the walk in global memory.
+            density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, ka, rho, status);
+            if (s1 != s0) density_at<kIndirect, false>(parts, ordenado, inicios, g, h2, n, kb, rho, status);
+            continue;
+        }
+        rho[ka] = acc[rd][0];
+        if (s1 != s0) rho[kb] = acc[rd][1];
+    }
+}
+
 // Linear order, one CTA per run of kTileCells cells of one row (see above).
 template <bool kIndirect>
 __global__ void __launch_bounds__(kTileThreads, kTileMinBlocks)
@@ -264,6 +380,7 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
     __shared__ uint32_t s_start[kStagedRows][kRowCells + 1];     // stage offset of each cell of each row, and the end
     __shared__ uint32_t s_first[kStagedRows];                    // cell-order index of each row's first candidate
     __shared__ uint32_t s_total;
+    __shared__ uint32_t s_sliced;                                // the candidates fit plane by plane only
     __shared__ uint32_t s_items[kTileRows * kTileCells + 1];     // first work item of each own cell, and the end
     allow_dependent_launch();
     grid_dependency_wait();
@@ -292,16 +409,21 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
     __syncthreads();
     if (tid == 0) {
         uint32_t base = 0;
-        bool fits = true;
+        bool fits = true, mono = true;
+        uint32_t plane[3] = {0u, 0u, 0u};  // candidates of each z plane (saturating)
         for (uint32_t r = 0; r < kStagedRows; ++r) {
             const uint32_t size = s_start[r][nc];
             // starts that decrease (inconsistent input) go to the walk, too
-            for (uint32_t c = 1; c <= nc; ++c) fits &= s_start[r][c] >= s_start[r][c - 1];
+            for (uint32_t c = 1; c <= nc; ++c) mono &= s_start[r][c] >= s_start[r][c - 1];
             if (size > kStageMax || base + size > kStageMax) fits = false;
+            const uint32_t p = r / (kTileRows + 2);
+            plane[p] = plane[p] + size < plane[p] ? 0xffffffffu : plane[p] + size;
             for (uint32_t c = 0; c <= nc; ++c) s_start[r][c] += base;
             base += size;
         }
+        fits &= mono;
         s_total = fits ? base : 0xffffffffu;
+        s_sliced = !fits && mono && plane[0] <= kStageMax && plane[1] <= kStageMax && plane[2] <= kStageMax;
         // One work item per two particles of an own cell (an odd last one alone).
         uint32_t items = 0, q = 0;
         for (uint32_t t = 0; t < rows; ++t) {
@@ -312,9 +434,15 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
             }
         }
         s_items[q] = items;
+        if (items > kSliceRounds * kTileThreads) s_sliced = 0u;
     }
     __syncthreads();
     const uint32_t total = s_total;
+    if (total == 0xffffffffu && s_sliced) {
+        tile_by_planes<kIndirect>(parts, ordenado, inicios, g, h2, n, rho, status, s_stage, s_start, s_first,
+                                  s_items, x0, x1, xa, y0, z, rows);
+        return;
+    }
     if (total == 0xffffffffu) {
         // The candidates do not fit: each own particle walks global memory.
         for (uint32_t t = 0; t < rows; ++t) {

@@ -31,6 +31,8 @@ stress          16,777,216  256^3      uniform; built 10 times, ping-pong
 sph             5,242,880   64^3       uniform; 20 per cell, ~84 neighbours
                                        within one cell size, records (168 MB)
                                        above L2: for the neighbour query
+sph_dense       13,107,200  64^3       uniform; 50 per cell (the dense
+                                       neighbour query), records 420 MB
 =============== =========== ========== =========================================
 """
 from __future__ import annotations
@@ -103,6 +105,10 @@ SCENES: dict[str, Scene] = {
         # cuesta la indirección).  Power-of-two sides, so it also builds in
         # Morton order.
         Scene("sph", 5_242_880, (64, 64, 64), seed_index=5),
+        # 50 particles per cell, near the top of the 20-60 per cell that
+        # "Contar partículas por celda" calls healthy: the dense neighbour
+        # query.  Records 420 MB, above L2.
+        Scene("sph_dense", 13_107_200, (64, 64, 64), seed_index=6),
     )
 }
 
