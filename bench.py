@@ -479,13 +479,13 @@ def run_gpu(args) -> None:
                       torch.cuda.current_stream())
 
     def settle(k, cold=True):
-        """Untimed: flush L2 (unless warm), then hold the stream briefly so
-        that the host has enqueued the whole step before the GPU reaches its
-        start event."""
+        """Untimed: flush L2 (unless warm), then hold the stream (~100 us of
+        spinning on the GPU) so that the host has enqueued the whole step
+        before the GPU reaches its start event."""
         if cold:
             flush.fill_(k & 0x7F)
         if sleep is not None:
-            sleep(40_000)
+            sleep(200_000)
 
     def timed(run, steps, cold=True):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -697,6 +697,7 @@ def run_gpu(args) -> None:
                             "traffic": kernel_traffic(["reorder.cu"]) if scene.name == TRAFFIC_SCENE else None},
         "build_hbm": {"algorithmic_bytes": total_alg, "us_per_build": ms_per_step * 1e3,
                       "us_min": 1e3 * min(step_ms), "us_median": 1e3 * statistics.median(step_ms),
+                      "us_max": 1e3 * max(step_ms), "us_steps": [round(1e3 * t, 2) for t in step_ms[:200]],
                       "achieved_gbs": gbs(ms_per_step * 1e3),
                       "frac_of_nominal_8tbs": gbs(ms_per_step * 1e3) / NOMINAL_HBM_GBS,
                       "frac_of_measured": gbs(ms_per_step * 1e3) / peak},

@@ -531,6 +531,97 @@ static_assert(kMortonStageMax % 2 == 0, "the Morton tile stages candidates in pa
 
 __host__ __device__ __forceinline__ uint32_t morton_block_side(uint32_t dim) { return dim < 4u ? dim : 4u; }
 
+// A Morton block whose box fits in shared memory one z plane at a time only
+// (denser scenes): the box's planes are staged one after the other (each
+// plane's cells are one stretch of the box order, which keeps z slowest), and
+// every particle of the block (up to kMortonRounds per thread) adds, in
+// registers, the rows of each plane within one cell of its own.  A particle
+// not in the block's cells takes the walk in global memory.
+constexpr uint32_t kMortonRounds = 8;
+template <bool kIndirect>
+__device__ __noinline__ void morton_by_planes(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
+                                                 const uint32_t *__restrict__ inicios, const Geometry &g, float h2,
+                                                 uint32_t n, float *__restrict__ rho, uint32_t *status,
+                                                 float4 *s_stage, const uint32_t *s_box, const uint32_t *s_first,
+                                                 uint32_t x0, uint32_t y0, uint32_t z0, uint32_t sx, uint32_t sy,
+                                                 uint32_t sz, uint32_t xa, uint32_t ya, uint32_t za, uint32_t nx,
+                                                 uint32_t ny, uint32_t nz, uint32_t k0, uint32_t k1) {
+    const uint32_t X = g.dims[0], Y = g.dims[1], Z = g.dims[2];
+    const uint32_t tid = threadIdx.x;
+    const uint32_t per_plane = nx * ny;
+    const float2 nh2v = make_float2(-h2, -h2);
+    float acc[kMortonRounds];
+#pragma unroll
+    for (uint32_t rd = 0; rd < kMortonRounds; ++rd) acc[rd] = 0.0f;
+    for (uint32_t iz = 0; iz < nz; ++iz) {
+        const uint32_t c_lo = iz * per_plane, c_hi = c_lo + per_plane;
+        const uint32_t pbase = s_box[c_lo], psize = s_box[c_hi] - pbase;
+        const uint32_t zz = za + iz;
+        __syncthreads();  // the previous plane's stage has been read
+        for (uint32_t i = tid; i < psize; i += kMortonThreads) {
+            uint32_t lo = c_lo, hi = c_hi;  // s_box[lo] <= pbase + i < s_box[hi]
+            while (hi - lo > 1) {
+                const uint32_t mid = (lo + hi) >> 1;
+                if (s_box[mid] <= pbase + i)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+            const uint32_t j = s_first[lo] + (pbase + i - s_box[lo]);
+            bool bad = j >= n;
+            const float4 q =
+                bad ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : candidate<kIndirect>(parts, ordenado, j, n, bad);
+            if (bad) record_status(status, kStatusBounds);
+            stage_put(s_stage, i, q);
+        }
+        __syncthreads();
+#pragma unroll
+        for (uint32_t rd = 0; rd < kMortonRounds; ++rd) {
+            const uint32_t k = k0 + tid + rd * kMortonThreads;
+            if (k >= k1) continue;
+            bool bad = false;
+            const float4 me = candidate<kIndirect>(parts, ordenado, k, n, bad);
+            if (bad) continue;
+            const uint32_t cx = axis_coord(me.x, g.origin[0], g.inv_cell, X);
+            const uint32_t cy = axis_coord(me.y, g.origin[1], g.inv_cell, Y);
+            const uint32_t cz = axis_coord(me.z, g.origin[2], g.inv_cell, Z);
+            if (cx < x0 || cx >= x0 + sx || cy < y0 || cy >= y0 + sy || cz < z0 || cz >= z0 + sz) continue;
+            if (zz + 1 < cz || zz > cz + 1) continue;  // this plane is not one of the particle's three
+            const float2 npx = make_float2(-me.x, -me.x), npy = make_float2(-me.y, -me.y);
+            const float2 npz = make_float2(-me.z, -me.z);
+            float2 n01 = make_float2(-0.0f, -0.0f), n23 = make_float2(-0.0f, -0.0f);
+            const uint32_t xl = (cx > 0 ? cx - 1 : 0u) - xa, xh = (cx + 1 < X ? cx + 1 : cx) - xa;
+#pragma unroll 1
+            for (int dy = -1; dy <= 1; ++dy) {
+                const int64_t yy = (int64_t)cy + dy;
+                if (yy < 0 || yy >= (int64_t)Y) continue;
+                const uint32_t row = c_lo + nx * ((uint32_t)yy - ya);
+                walk_range(s_stage, s_box[row + xl] - pbase, s_box[row + xh + 1] - pbase, me, npx, npy, npz, nh2v,
+                           n01, n23);
+            }
+            acc[rd] += -((n01.x + n01.y) + (n23.x + n23.y));
+        }
+    }
+#pragma unroll
+    for (uint32_t rd = 0; rd < kMortonRounds; ++rd) {
+        const uint32_t k = k0 + tid + rd * kMortonThreads;
+        if (k >= k1) continue;
+        bool bad = false;
+        const float4 me = candidate<kIndirect>(parts, ordenado, k, n, bad);
+        if (bad) {
+            record_status(status, kStatusBounds);
+            continue;
+        }
+        const uint32_t cx = axis_coord(me.x, g.origin[0], g.inv_cell, X);
+        const uint32_t cy = axis_coord(me.y, g.origin[1], g.inv_cell, Y);
+        const uint32_t cz = axis_coord(me.z, g.origin[2], g.inv_cell, Z);
+        if (cx < x0 || cx >= x0 + sx || cy < y0 || cy >= y0 + sy || cz < z0 || cz >= z0 + sz)
+            density_at<kIndirect, true>(parts, ordenado, inicios, g, h2, n, k, rho, status);
+        else
+            rho[k] = acc[rd];
+    }
+}
+
 template <bool kIndirect>
 __global__ void __launch_bounds__(kMortonThreads, kMortonMinBlocks)
 density_morton_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict__ ordenado,
@@ -540,6 +631,7 @@ density_morton_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__re
     __shared__ uint32_t s_box[kBoxMax + 1];      // stage offset of each box cell, and the end
     __shared__ uint32_t s_first[kBoxMax];        // cell-order index of each box cell's first particle
     __shared__ uint32_t s_total;
+    __shared__ uint32_t s_sliced;                // the box fits z plane by z plane only
     allow_dependent_launch();
     grid_dependency_wait();
     const uint32_t X = g.dims[0], Y = g.dims[1], Z = g.dims[2];
@@ -561,21 +653,37 @@ density_morton_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__re
     }
     __syncthreads();
     if (tid == 0) {
+        // Offsets over the whole box while it fits; past that, offsets
+        // within each z plane, as long as every plane fits (then the block
+        // is staged plane by plane).
         uint32_t sum = 0;
-        bool fits = true;
-        for (uint32_t i = 0; i < ncell; ++i) {
-            const uint32_t size = s_box[i];
-            if (size > kMortonStageMax || sum + size > kMortonStageMax) fits = false;
-            s_box[i] = sum;
-            sum += fits ? size : 0u;
+        bool fits = true, planes = true;
+        const uint32_t per_plane = nx * ny;
+        for (uint32_t iz = 0; iz < nz; ++iz) {
+            uint32_t psum = 0;
+            for (uint32_t i = iz * per_plane; i < (iz + 1) * per_plane; ++i) {
+                const uint32_t size = s_box[i];
+                if (size > kMortonStageMax || psum + size > kMortonStageMax) planes = false;
+                if (size > kMortonStageMax || sum + size > kMortonStageMax) fits = false;
+                s_box[i] = sum;
+                const uint32_t add = size > kMortonStageMax ? 0u : size;
+                sum += add;
+                psum += add;
+            }
         }
         s_box[ncell] = sum;
         s_total = fits ? sum : 0xffffffffu;
+        s_sliced = !fits && planes;
     }
     __syncthreads();
     const uint32_t total = s_total;
     const uint32_t c0 = cell_at(x0, y0, z0, g);
     const uint32_t k0 = __ldg(inicios + c0), k1 = min(__ldg(inicios + c0 + sx * sy * sz), n);
+    if (total == 0xffffffffu && s_sliced && k1 >= k0 && k1 - k0 <= kMortonRounds * kMortonThreads) {
+        morton_by_planes<kIndirect>(parts, ordenado, inicios, g, h2, n, rho, status, s_stage, s_box, s_first, x0,
+                                    y0, z0, sx, sy, sz, xa, ya, za, nx, ny, nz, k0, k1);
+        return;
+    }
     if (total == 0xffffffffu) {
         for (uint32_t k = k0 + tid; k < k1; k += kMortonThreads)
             density_at<kIndirect, true>(parts, ordenado, inicios, g, h2, n, k, rho, status);
