@@ -216,29 +216,52 @@ __device__ __forceinline__ void gather_bucket(const CUtensorMap *map, const Buil
     }
 }
 
+// Bands for pairs_from_celdaDe.  Each stretch a CTA writes keeps about two
+// partly written 128-byte lines open (its first and its last) until it is
+// full; with every CTA's stretches like this one's (`touched` buckets),
+// enough bands that one band's open lines take at most kBandBytes of L2.
+// Input already in cell order touches few buckets per CTA: one band.
+constexpr uint64_t kBandBytes = 96ull << 20;
+__device__ __forceinline__ uint32_t pair_bands(uint32_t touched, uint32_t ctas) {
+    const uint64_t open = (uint64_t)ctas * touched * 2 * 128;
+    const uint64_t bands = (open + kBandBytes - 1) / kBandBytes;
+    return (uint32_t)max((uint64_t)1, min(bands, (uint64_t)64));
+}
+
 // Phase C's pairs when phase A could not keep the CTA's cells and ranks
 // (more particles per CTA than its cache holds): cells re-read from celdaDe,
-// places taken from the shared cursors.  Out of line: on the common sizes it
-// never runs, and its code stays out of the way of the code that does.
+// places taken from the shared cursors.  The writes are scattered 8-byte
+// stores into every CTA's stretch of every bucket; when those stretches are
+// too many for their partly written lines to stay in L2 until they fill,
+// the lines go to DRAM half written.  So the buckets are taken in `bands`
+// passes of consecutive buckets, each pass re-reading celdaDe and writing
+// only the pairs of its band: a band's open lines fit in L2.  Out of line:
+// on the common sizes it never runs, and its code stays out of the way of
+// the code that does.
 __device__ __noinline__ void pairs_from_celdaDe(const BuildArgs a, const BucketScratch bk, uint32_t *s_table,
-                                                uint64_t p_lo, uint64_t p_hi, uint32_t *status) {
-    for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
-        uint32_t cell[kScatterItems];
+                                                uint64_t p_lo, uint64_t p_hi, uint32_t bands, uint32_t *status) {
+    const uint32_t per_band = (bk.buckets + bands - 1) / bands;
+    for (uint32_t band = 0; band < bands; ++band) {
+        const uint32_t b_lo = band * per_band, b_hi = min(bk.buckets, b_lo + per_band);
+        for (uint64_t r0 = p_lo; r0 < p_hi; r0 += (uint64_t)kThreads * kScatterItems) {
+            uint32_t cell[kScatterItems];
 #pragma unroll
-        for (int k = 0; k < kScatterItems; ++k) {
-            const uint64_t i = r0 + (uint64_t)k * kThreads + threadIdx.x;
-            if (i < p_hi) cell[k] = a.celdaDe[i];
-        }
+            for (int k = 0; k < kScatterItems; ++k) {
+                const uint64_t i = r0 + (uint64_t)k * kThreads + threadIdx.x;
+                if (i < p_hi) cell[k] = a.celdaDe[i];
+            }
 #pragma unroll
-        for (int k = 0; k < kScatterItems; ++k) {
-            const uint64_t i = r0 + (uint64_t)k * kThreads + threadIdx.x;
-            const bool valid = i < p_hi;
-            const uint32_t q = smem_take(s_table, valid, valid ? bucket_of(cell[k], bk) : 0u);
-            if (valid) {
-                if (q < a.n)
-                    bk.pairs[q] = make_uint2(cell[k], (uint32_t)i);
-                else
-                    record_status(status, kStatusBounds);
+            for (int k = 0; k < kScatterItems; ++k) {
+                const uint64_t i = r0 + (uint64_t)k * kThreads + threadIdx.x;
+                const uint32_t b = i < p_hi ? bucket_of(cell[k], bk) : 0u;
+                const bool valid = i < p_hi && b >= b_lo && b < b_hi;
+                const uint32_t q = smem_take(s_table, valid, valid ? b : 0u);
+                if (valid) {
+                    if (q < a.n)
+                        bk.pairs[q] = make_uint2(cell[k], (uint32_t)i);
+                    else
+                        record_status(status, kStatusBounds);
+                }
             }
         }
     }
@@ -289,6 +312,7 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
     __shared__ uint32_t s_red[kWarps];
     __shared__ uint32_t s_rows[kScanVecs + 1][kWarps];  // + the rows' totals
     __shared__ uint32_t s_clean, s_bclean, s_base, s_count, s_nlong;
+    __shared__ uint32_t s_touched;  // buckets this CTA has particles in
     __shared__ uint32_t s_own_base[kOwnMax], s_own_count[kOwnMax];
     __shared__ __align__(8) unsigned long long s_gbar[kWarps];  // one per warp, phase D's gather
     __shared__ uint32_t s_long[kLongMax];  // stable mode: cells of the bucket with more than 32 particles
@@ -303,6 +327,7 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
     if (tid == 0) {
         s_clean = *reinterpret_cast<volatile uint32_t *>(&hdr->counts_clean) >= a.cells;
         s_bclean = *reinterpret_cast<volatile uint32_t *>(&hdr->buckets_clean) != 0u;
+        s_touched = 0u;
     }
 #pragma unroll
     for (int q = 0; q < kScanVecs; ++q) s_held[q][tid] = make_uint4(0u, 0u, 0u, 0u);  // s_table, 8192 words
@@ -358,11 +383,14 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
     __syncthreads();
     // This CTA's stretch within its lane of every bucket it has particles in:
     // the atomic's old value is the offset, and the lane words end as totals.
+    uint32_t touched = 0;
     for (uint32_t b = tid; b < B; b += kThreads) {
         const uint32_t m = s_table[b];
         if (grouped) s_table[B + b] = m;  // the histogram, kept for phase C
         if (m) s_table[b] = atomicAdd(bk.total + (uint64_t)b * kBucketLanes + blockIdx.x % kBucketLanes, m);
+        touched += m != 0u;
     }
+    if (!cached && touched) atomicAdd(&s_touched, touched);
     grid_arrive(hdr, passed);
     if (grouped) {
         // Phase C writes this CTA's pairs as runs of consecutive positions,
@@ -494,7 +522,7 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
                     record_status(&hdr->status, kStatusBounds);
             }
         } else {
-            pairs_from_celdaDe(a, bk, s_table, p_lo, p_hi, &hdr->status);
+            pairs_from_celdaDe(a, bk, s_table, p_lo, p_hi, pair_bands(s_touched, ctas), &hdr->status);
         }
         grid_arrive(hdr, passed);
         // The first bucket's cell table is cleared while the barrier fills.
