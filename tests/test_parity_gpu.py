@@ -63,6 +63,91 @@ def test_ragged(ug, oracle_lib, n, dims, stable):
     _check(ug, oracle_lib, rows, dims, origin, cs, stable)
 
 
+# ---------------------------------------------------------------- small scenes (one-CTA build)
+
+SMALL = [(8192, (32, 16, 16)), (8193, (32, 16, 16)), (8192, (3, 2731, 1)), (5000, (20, 20, 20)),
+         (7, (1, 1, 1)), (8192, (1, 1, 1)), (3000, (7, 5, 3))]
+
+
+@pytest.mark.parametrize("stable", [False, True], ids=["atomic", "stable"])
+@pytest.mark.parametrize("n,dims", SMALL, ids=[f"{n}-{d[0]}x{d[1]}x{d[2]}" for n, d in SMALL])
+def test_small_scene_limits(ug, oracle_lib, n, dims, stable):
+    """Scenes at, just past and far inside the one-CTA build's limits (8192
+    particles, 8192 cells): 8192 cells, 8193 particles, 8193 cells, a cell
+    count that is not a multiple of eight, every particle in one cell."""
+    origin = (np.float32(-0.9), np.float32(0.4), np.float32(-2.1))
+    cs = np.float32(0.25)
+    rng = np.random.default_rng(n + dims[0])
+    lo = np.array(origin, np.float64) - 0.3
+    hi = np.array(origin, np.float64) + np.array(dims) * float(cs) + 0.3
+    rows = np.zeros((n, 8), np.float32)
+    rows[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+    rows[:, 3:] = rng.random((n, 5)).astype(np.float32)
+    _check(ug, oracle_lib, rows, dims, origin, cs, stable)
+
+
+@pytest.mark.parametrize("crowd", [33, 1024, 1025, 6000])
+def test_small_scene_long_segments(ug, oracle_lib, crowd):
+    """A small scene with one crowded cell among scattered particles: the
+    one-CTA build's stable mode sorts segments longer than 32 with the whole
+    CTA."""
+    rng = np.random.default_rng(crowd)
+    base = scenes.uniform_particles(8000 - crowd, 41)
+    rows = np.concatenate([base, base[:crowd].copy()])
+    rows[-crowd:, :3] = np.float32(0.1)
+    rows = rows[rng.permutation(rows.shape[0])]
+    for stable in (True, False):
+        _check(ug, oracle_lib, rows, (16,) * 3, (-5.0,) * 3, 0.625, stable)
+
+
+# ---------------------------------------------------------------- sparse grids (single-barrier build)
+
+SPARSE = [(5_000, (97, 89, 13)), (20_000, (256, 256, 3)), (100_000, (128, 128, 128)),
+          (200_000, (256, 256, 256)), (250_000, (1024, 1024, 3)), (300_001, (512, 512, 9)),
+          (9_000, (200, 100, 50))]
+
+
+@pytest.mark.parametrize("stable", [False, True], ids=["atomic", "stable"])
+@pytest.mark.parametrize("n,dims", SPARSE, ids=[f"{n}-{d[0]}x{d[1]}x{d[2]}" for n, d in SPARSE])
+def test_sparse_grids(ug, oracle_lib, n, dims, stable):
+    """At least four cells per particle: buckets of one window and of several
+    (256^3 over the CTAs is about 55,000 cells a bucket, 1024 x 1024 x 3 about
+    10,000), ragged sides."""
+    origin = (np.float32(-3.1), np.float32(0.6), np.float32(-0.2))
+    cs = np.float32(0.05)
+    rng = np.random.default_rng(n + 7)
+    lo = np.array(origin, np.float64) - 0.2
+    hi = np.array(origin, np.float64) + np.array(dims) * float(cs) + 0.2
+    rows = np.zeros((n, 8), np.float32)
+    rows[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+    rows[:, 3:] = rng.random((n, 5)).astype(np.float32)
+    _check(ug, oracle_lib, rows, dims, origin, cs, stable)
+
+
+@pytest.mark.parametrize("crowd", [5_000, 12_000, 40_000])
+def test_sparse_grid_crowded_bucket(ug, oracle_lib, crowd):
+    """A sparse grid whose crowded cell puts more particles in one bucket than
+    a CTA holds: that bucket streams its pairs (and, in stable mode, sorts the
+    crowded segment in shared memory or by radix)."""
+    rng = np.random.default_rng(crowd)
+    base = scenes.uniform_particles(100_000 - crowd, 43)
+    rows = np.concatenate([base, base[:crowd].copy()])
+    rows[-crowd:, :3] = np.float32(1.01)
+    rows[-crowd // 3:, :3] = np.float32(1.09)  # a second crowded cell next to it
+    rows = rows[rng.permutation(rows.shape[0])]
+    for stable in (True, False):
+        _check(ug, oracle_lib, rows, (128,) * 3, (-5.0,) * 3, 0.078125, stable)
+
+
+def test_sparse_grid_morton(ug, oracle_lib):
+    rows = scenes.uniform_particles(150_000, 47)
+    p = ug.make_params(rows.shape[0], (128,) * 3, (-5.0,) * 3, 0.078125, order=ug.GRID_ORDER_MORTON)
+    ref = oracle_lib.build(rows, (128,) * 3, (-5.0,) * 3, 0.078125, order=1)
+    for stable in (False, True):
+        got = gpu_build(ug, rows, (128,) * 3, (-5.0,) * 3, 0.078125, ug.GRID_STABLE if stable else 0, params=p)
+        assert_matches_oracle(oracle_lib, rows, got, ref, stable)
+
+
 # ---------------------------------------------------------------- cell-index edge cases
 
 @pytest.mark.parametrize("dims,cs", [((16,) * 3, 0.625), ((128,) * 3, 0.078125), ((256,) * 3, 0.0390625),

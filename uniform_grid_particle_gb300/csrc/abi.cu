@@ -241,6 +241,21 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
     grid_ws_header *h = header(ws);
     char *base = static_cast<char *>(ws);
     const bool stable = (flags & GRID_STABLE) != 0;
+    if (n != 0 && n <= kSmallMaxParticles && c <= kSmallMaxCells) {
+        // A small scene: the whole build in one CTA (build_small.cu).
+        return cuda_code(launch_build_small(origen, destino, conteos, celdaDe, inicios, ordenado, (uint32_t)n,
+                                            (uint32_t)c, g, stable, st));
+    }
+    if (n != 0 && n * kSparseCellsPerParticle <= c) {
+        // A sparse grid: one exchange between the particles' CTAs and the
+        // cells' CTAs, one grid barrier (build_sparse.cu).
+        const cudaError_t f = launch_build_sparse(
+            origen, destino, conteos, celdaDe, inicios, ordenado, (uint32_t)n, c, g, h,
+            reinterpret_cast<uint32_t *>(base + l.counts), reinterpret_cast<uint32_t *>(base + l.pairs), stable,
+            stable ? reinterpret_cast<uint32_t *>(base + l.stable_scratch) : nullptr, st);
+        if (f != cudaErrorNotSupported) return cuda_code(f);
+        (void)cudaGetLastError();
+    }
     if (n != 0) {
         // The two-level counting sort in one cooperative launch (build_bucketed.cu).
         const cudaError_t f = launch_build_bucketed(

@@ -71,7 +71,7 @@ constexpr int kMaxDevices = 64;
 // kBucketCap / (kRegisterMax + 1) of them fit in a bucket.
 constexpr uint32_t kLongMax = kBucketCap / (kRegisterMax + 1) + 1;
 // The first buckets a CTA places: phase C keeps their bases and sizes in
-// shared memory when the buckets fit one scan row (any others are read back).
+// shared memory (any others are read back from the workspace).
 constexpr uint32_t kOwnMax = 32;
 // Phase D's gather: records per warp chunk (four per lane) and the stage bytes.
 constexpr uint32_t kGatherChunk = 128;
@@ -112,40 +112,6 @@ __device__ __forceinline__ uint32_t bucket_total(const uint32_t *total, uint32_t
 __device__ __forceinline__ void zero_bucket(uint32_t *total, uint32_t b) {
     uint4 *t = reinterpret_cast<uint4 *>(total + (uint64_t)b * kBucketLanes);
     t[0] = t[1] = make_uint4(0u, 0u, 0u, 0u);
-}
-
-// Shared-memory add of 1 to table[key] for every valid lane; returns the
-// value before this lane's add.  Lanes of a warp that share a key are served
-// by one atomic of their leader when the cheap adjacent-duplicate test finds
-// any, so crowded keys do not serialise.  When the valid lanes are a prefix of
-// the warp and their keys do not decrease (input already in cell order), the
-// runs of equal keys are found with one ballot: each run's first lane adds
-// the run's length.  Otherwise __match_any_sync groups the lanes.
-__device__ __forceinline__ uint32_t smem_take(uint32_t *table, bool valid, uint32_t key) {
-    if (!warp_has_adjacent_duplicates(valid, key)) return valid ? atomicAdd(&table[key], 1u) : 0u;
-    const uint32_t lane = lane_id();
-    const uint32_t active = __ballot_sync(0xffffffffu, valid);
-    const uint32_t below = __shfl_up_sync(0xffffffffu, key, 1);
-    const bool prefix = (active & (active + 1u)) == 0u;  // lanes 0..k-1 valid, the rest not
-    if (prefix && __all_sync(0xffffffffu, !valid || lane == 0 || below <= key)) {
-        const uint32_t heads = __ballot_sync(0xffffffffu, valid && (lane == 0 || below != key));
-        const uint32_t upto = lane == 31 ? 0xffffffffu : (2u << lane) - 1u;
-        const uint32_t start = 31u - (uint32_t)__clz(heads & upto);
-        const uint32_t later = (heads | ~active) & ~upto;  // the next run's head, or the first invalid lane
-        const uint32_t end = later ? (uint32_t)(__ffs(later) - 1) : 32u;
-        uint32_t first = 0u;
-        if (valid && lane == start) first = atomicAdd(&table[key], end - start);
-        first = __shfl_sync(0xffffffffu, first, start);
-        return valid ? first + (lane - start) : 0u;
-    }
-    uint32_t first = 0u, peers = 0u;
-    if (valid) {
-        peers = __match_any_sync(active, key);
-        const uint32_t leader = (uint32_t)(__ffs(peers) - 1);
-        if (lane == leader) first = atomicAdd(&table[key], (uint32_t)__popc(peers));
-        first = __shfl_sync(peers, first, leader);
-    }
-    return first + (uint32_t)__popc(peers & lanemask_lt());
 }
 
 // Phase D's record move for one bucket (destino[base + q] = origen[s_order[q]],
@@ -480,13 +446,26 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
                 }
                 // The buckets this CTA places in phase D, blockIdx.x + j * ctas:
                 // their bases and sizes, from the thread that holds them.
-                if (q == 0 && B <= 4u * kThreads) {
-                    for (uint32_t j = 0, bj = blockIdx.x; bj < B && j < kOwnMax; ++j, bj += ctas) {
-                        if ((bj >> 2) == tid) {
-                            const uint32_t e = bj & 3u;
-                            s_own_base[j] = e == 0 ? start[0] : e == 1 ? start[1] : e == 2 ? start[2] : start[3];
-                            s_own_count[j] = e == 0 ? size[0] : e == 1 ? size[1] : e == 2 ? size[2] : size[3];
+                if (B <= 4u * kThreads) {
+                    // One row of buckets: the thread that holds bucket bj.
+                    if (q == 0) {
+                        for (uint32_t j = 0, bj = blockIdx.x; bj < B && j < kOwnMax; ++j, bj += ctas) {
+                            if ((bj >> 2) == tid) {
+                                const uint32_t e = bj & 3u;
+                                s_own_base[j] = e == 0 ? start[0] : e == 1 ? start[1] : e == 2 ? start[2] : start[3];
+                                s_own_count[j] = e == 0 ? size[0] : e == 1 ? size[1] : e == 2 ? size[2] : size[3];
+                            }
                         }
+                    }
+                } else if (b0 < B && ctas >= 4u) {
+                    // Several rows: at most one of this thread's four buckets
+                    // is one this CTA places (ctas >= 4 apart).
+                    const uint32_t jj = b0 + 3u >= blockIdx.x ? (b0 + 3u - blockIdx.x) / ctas : kOwnMax;
+                    const uint32_t bj = blockIdx.x + jj * ctas;
+                    if (jj < kOwnMax && bj >= b0 && bj < b0 + 4u && bj < B) {
+                        const uint32_t e = bj - b0;
+                        s_own_base[jj] = e == 0 ? start[0] : e == 1 ? start[1] : e == 2 ? start[2] : start[3];
+                        s_own_count[jj] = e == 0 ? size[0] : e == 1 ? size[1] : e == 2 ? size[2] : size[3];
                     }
                 }
                 row_base += rows[q];
@@ -537,7 +516,7 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
             if (tid == 0) {
                 s_nlong = 0u;
                 s_nmulti = 0u;
-                if (B <= 4u * kThreads && j < kOwnMax) {
+                if (j < kOwnMax && (B <= 4u * kThreads || ctas >= 4u)) {
                     s_base = s_own_base[j];
                     s_count = s_own_count[j];
                 } else {

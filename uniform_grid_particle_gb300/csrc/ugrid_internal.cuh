@@ -154,6 +154,32 @@ cudaError_t launch_build_bucketed(const ugrid_particula *origen, ugrid_particula
                                   uint32_t *pairs, bool stable, uint32_t *queue, uint32_t queue_capacity,
                                   uint32_t *sort_scratch, cudaStream_t s);
 
+// The whole build in one CTA, for scenes of at most kSmallMaxParticles
+// particles on at most kSmallMaxCells cells (see build_small.cu).
+// The sparse build: at most this many particles per CTA of its launch
+// (measured: with more, its plain-load gather and its phase 1 make it slower
+// than the bucketed build).
+constexpr uint32_t kSparseMaxParticlesPerCta = 1024;
+// grid_build takes the sparse build when there are at least this many cells
+// per particle.
+constexpr uint64_t kSparseCellsPerParticle = 4;
+constexpr uint32_t kSmallMaxParticles = 8192;
+constexpr uint32_t kSmallMaxCells = 8192;
+cudaError_t launch_build_small(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
+                               uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, uint32_t n,
+                               uint32_t cells, const Geometry &g, bool stable, cudaStream_t s);
+
+// The build for sparse grids, one cooperative launch with one grid barrier
+// (see build_sparse.cu).  Its table of per-CTA bucket offsets lives in the
+// fused build's counter array `counts` (the kernel marks it not clean).
+// Returns cudaErrorNotSupported, having launched nothing, when a CTA's
+// particles would not fit (n > grid * kSparseMaxParticlesPerCta) or the table
+// would not fit in `cells` words.
+cudaError_t launch_build_sparse(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
+                                uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, uint32_t n, uint64_t cells,
+                                const Geometry &g, grid_ws_header *hdr, uint32_t *counts, uint32_t *pairs,
+                                bool stable, uint32_t *sort_scratch, cudaStream_t s);
+
 // Several arrays gathered with one ordenado (grid_reorder_many).
 constexpr int kMaxArrays = 4;
 struct ManyArrays {
@@ -262,6 +288,40 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
+}
+
+// Shared-memory add of 1 to table[key] for every valid lane; returns the
+// value before this lane's add.  Lanes of a warp that share a key are served
+// by one atomic of their leader when the cheap adjacent-duplicate test finds
+// any, so crowded keys do not serialise.  When the valid lanes are a prefix of
+// the warp and their keys do not decrease (input already in cell order), the
+// runs of equal keys are found with one ballot: each run's first lane adds
+// the run's length.  Otherwise __match_any_sync groups the lanes.
+__device__ __forceinline__ uint32_t smem_take(uint32_t *table, bool valid, uint32_t key) {
+    if (!warp_has_adjacent_duplicates(valid, key)) return valid ? atomicAdd(&table[key], 1u) : 0u;
+    const uint32_t lane = lane_id();
+    const uint32_t active = __ballot_sync(0xffffffffu, valid);
+    const uint32_t below = __shfl_up_sync(0xffffffffu, key, 1);
+    const bool prefix = (active & (active + 1u)) == 0u;  // lanes 0..k-1 valid, the rest not
+    if (prefix && __all_sync(0xffffffffu, !valid || lane == 0 || below <= key)) {
+        const uint32_t heads = __ballot_sync(0xffffffffu, valid && (lane == 0 || below != key));
+        const uint32_t upto = lane == 31 ? 0xffffffffu : (2u << lane) - 1u;
+        const uint32_t start = 31u - (uint32_t)__clz(heads & upto);
+        const uint32_t later = (heads | ~active) & ~upto;  // the next run's head, or the first invalid lane
+        const uint32_t end = later ? (uint32_t)(__ffs(later) - 1) : 32u;
+        uint32_t first = 0u;
+        if (valid && lane == start) first = atomicAdd(&table[key], end - start);
+        first = __shfl_sync(0xffffffffu, first, start);
+        return valid ? first + (lane - start) : 0u;
+    }
+    uint32_t first = 0u, peers = 0u;
+    if (valid) {
+        peers = __match_any_sync(active, key);
+        const uint32_t leader = (uint32_t)(__ffs(peers) - 1);
+        if (lane == leader) first = atomicAdd(&table[key], (uint32_t)__popc(peers));
+        first = __shfl_sync(peers, first, leader);
+    }
+    return first + (uint32_t)__popc(peers & lanemask_lt());
 }
 
 __device__ __forceinline__ unsigned long long global_ns() {
