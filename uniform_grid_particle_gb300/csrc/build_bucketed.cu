@@ -525,6 +525,12 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
                     s_count = bucket_total(bk.total, b, 0u, unused);
                 }
                 zero_bucket(bk.total, b);  // clean for the next build
+                // The next bucket's pairs, into L2 while this one is placed.
+                if (j + 1 < kOwnMax && b + ctas < B && (B <= 4u * kThreads || ctas >= 4u)) {
+                    const uint32_t nb = s_own_base[j + 1], nc = min(s_own_count[j + 1], kBucketCap);
+                    if (nb <= a.n && nc <= a.n - nb && nc != 0u)
+                        bulk_prefetch_l2(bk.pairs + nb, nc * (uint32_t)sizeof(uint2));
+                }
             }
             __syncthreads();
             const uint32_t base = s_base;
