@@ -339,14 +339,14 @@ __device__ __forceinline__ uint4 load_nc_na(const uint4 *p) {
     return v;
 }
 
-// The bytes [p, p + bytes) fetched into L2 by the bulk copy engine (p rounded
-// down and the end rounded up to 16 bytes: both must stay inside the
-// allocation, which holds for arrays of 8-byte elements that start 16-byte
-// aligned and end at least 8 bytes before the allocation does).
+// The bytes [p, p + bytes) fetched into L2 by the bulk copy engine: a hint,
+// over the 16-byte aligned part of the range only (the start rounded up and
+// the end rounded down), so it never touches a byte outside it.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
-    const uintptr_t lo = reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)15;
-    const uintptr_t hi = (reinterpret_cast<uintptr_t>(p) + bytes + 15) & ~(uintptr_t)15;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
+    const uintptr_t lo = (reinterpret_cast<uintptr_t>(p) + 15) & ~(uintptr_t)15;
+    const uintptr_t hi = (reinterpret_cast<uintptr_t>(p) + bytes) & ~(uintptr_t)15;
+    if (hi > lo)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
 }
 
 // 16-byte streaming store (evict-first).
