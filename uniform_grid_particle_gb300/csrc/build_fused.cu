@@ -75,7 +75,6 @@ build_fused_kernel(BuildArgs a, Geometry g, grid_ws_header *hdr, FusedScratch ws
     __shared__ uint32_t s_clean;
     __shared__ uint32_t s_rows[kScanVecs + 1][kWarps];  // + the rows' totals
     const uint32_t tid = threadIdx.x;
-    const uint32_t ctas = gridDim.x;
     uint32_t passed = 0;  // grid barriers passed (thread 0)
     // Read before this CTA's first arrival, hence before anyone changes it.
     if (tid == 0) s_clean = *reinterpret_cast<volatile uint32_t *>(&hdr->counts_clean) >= a.cells;
