@@ -86,6 +86,37 @@ def test_small_scene_limits(ug, oracle_lib, n, dims, stable):
     _check(ug, oracle_lib, rows, dims, origin, cs, stable)
 
 
+CLUSTER = [(32_768, (64, 64, 32)), (32_769, (64, 64, 32)), (30_000, (50, 50, 50)), (20_000, (128, 1000, 1)),
+           (12_345, (131_073, 1, 1)), (20_000, (16, 16, 16))]
+
+
+@pytest.mark.parametrize("stable", [False, True], ids=["atomic", "stable"])
+@pytest.mark.parametrize("n,dims", CLUSTER, ids=[f"{n}-{d[0]}x{d[1]}x{d[2]}" for n, d in CLUSTER])
+def test_cluster_scene_limits(ug, oracle_lib, n, dims, stable):
+    """Scenes at and just past the cluster build's limits (32,768 particles,
+    131,072 cells), and inside them."""
+    origin = (np.float32(-0.5), np.float32(-0.25), np.float32(0.0))
+    cs = np.float32(0.125)
+    rng = np.random.default_rng(n + dims[1])
+    lo = np.array(origin, np.float64) - 0.2
+    hi = np.array(origin, np.float64) + np.array(dims) * float(cs) + 0.2
+    rows = np.zeros((n, 8), np.float32)
+    rows[:, :3] = (lo + (hi - lo) * rng.random((n, 3))).astype(np.float32)
+    rows[:, 3:] = rng.random((n, 5)).astype(np.float32)
+    _check(ug, oracle_lib, rows, dims, origin, cs, stable)
+
+
+@pytest.mark.parametrize("n", [8192, 32_768])
+def test_cluster_scene_one_cell(ug, oracle_lib, n):
+    """Every particle on one cell of a small grid: the cluster build's warps
+    take their slots with one remote atomic per warp."""
+    rows = scenes.single_cell_particles(n, 9, (0.3, 0.3, 0.3))
+    for stable in (False, True):
+        got = _check(ug, oracle_lib, rows, (16,) * 3, (-5.0,) * 3, 0.625, stable)
+        if stable:
+            assert np.array_equal(got["ordenado"], np.arange(n, dtype=np.uint32))
+
+
 @pytest.mark.parametrize("crowd", [33, 1024, 1025, 6000])
 def test_small_scene_long_segments(ug, oracle_lib, crowd):
     """A small scene with one crowded cell among scattered particles: the

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libugrid.so")
 
-SOURCES = ["abi.cu", "build_fused.cu", "build_bucketed.cu", "build_small.cu", "build_sparse.cu", "count.cu", "scan.cu", "scatter.cu", "reorder.cu", "segsort.cu",
+SOURCES = ["abi.cu", "build_fused.cu", "build_bucketed.cu", "build_small.cu", "build_cluster.cu", "build_sparse.cu", "count.cu", "scan.cu", "scatter.cu", "reorder.cu", "segsort.cu",
            "scan_noalloc.cu", "diagnostics.cu", "reorder_many.cu",
            "density.cu"]
 HEADERS = [os.path.join(CSRC, "ugrid_internal.cuh"), os.path.join(CSRC, "segsort_device.cuh"),

@@ -241,6 +241,13 @@ int grid_build(const ugrid_particula *origen, ugrid_particula *destino, uint32_t
     grid_ws_header *h = header(ws);
     char *base = static_cast<char *>(ws);
     const bool stable = (flags & GRID_STABLE) != 0;
+    if (n != 0 && !stable && n <= kClusterMaxParticles && c <= kClusterMaxCells) {
+        // A small scene, non-stable: one thread-block cluster (build_cluster.cu).
+        const cudaError_t f = launch_build_cluster(origen, destino, conteos, celdaDe, inicios, ordenado, (uint32_t)n,
+                                                   (uint32_t)c, g, st);
+        if (f != cudaErrorNotSupported) return cuda_code(f);
+        (void)cudaGetLastError();
+    }
     if (n != 0 && n <= kSmallMaxParticles && c <= kSmallMaxCells) {
         // A small scene: the whole build in one CTA (build_small.cu).
         return cuda_code(launch_build_small(origen, destino, conteos, celdaDe, inicios, ordenado, (uint32_t)n,
