@@ -168,9 +168,11 @@ __device__ __forceinline__ void store_four(uint32_t *conteos, uint64_t c, uint64
 }
 
 // One window of the bucket's cells [w0, w0 + kWindow): s_table holds their
-// counts.  Writes conteos and inicios (inicios = base + the bucket-local
-// start) and leaves the bucket-local starts in s_table; returns the window's
-// particles.  `run` is the bucket-local position of the window's first one.
+// counts.  Writes conteos (only the vectors of four that are not all zero:
+// the bucket's conteos were zeroed while the grid barrier filled) and inicios
+// (inicios = base + the bucket-local start), and leaves the bucket-local
+// starts in s_table; returns the window's particles.  `run` is the
+// bucket-local position of the window's first one.
 __device__ __forceinline__ uint32_t scan_window(uint32_t *conteos, uint32_t *inicios, uint32_t *s_table, uint64_t w0,
                                                 uint64_t hi, uint32_t run, uint32_t base,
                                                 uint32_t (*s_rows)[kWarps]) {
@@ -190,7 +192,7 @@ __device__ __forceinline__ uint32_t scan_window(uint32_t *conteos, uint32_t *ini
         const uint4 v = s_vec[q * kThreads + tid];
         const uint32_t first = row_base + excl[q];
         const uint64_t c = w0 + (uint64_t)q * kRowCells + 4u * tid;
-        store_four(conteos, c, hi, v);
+        if (v.x | v.y | v.z | v.w) store_four(conteos, c, hi, v);  // zeros written before the barrier
         fused::store_starts(inicios, c, hi, base + first, v);
         s_vec[q * kThreads + tid] = make_uint4(first, first + v.x, first + v.x + v.y, first + v.x + v.y + v.z);
         row_base += rows[q];
@@ -450,6 +452,16 @@ __global__ void __launch_bounds__(kThreads, 2) build_sparse_kernel(SparseArgs a,
     for (uint32_t i = tid; i < m; i += kThreads) a.pairs[p_lo + i] = s_pair[i];
 
     fused::grid_arrive(hdr, passed);
+    // While the barrier fills: conteos of this CTA's bucket set to zero, so
+    // that phase 2 writes only the counts that are not (most cells of a
+    // sparse grid are empty, and these stores overlap the wait).
+    if (blockIdx.x < a.buckets) {
+        const uint64_t lo = (uint64_t)blockIdx.x * a.width, hi = min(a.cells, lo + a.width);
+        uint4 *c4 = reinterpret_cast<uint4 *>(a.conteos + lo);
+        const uint64_t quads = (hi - lo) / 4;
+        for (uint64_t q = tid; q < quads; q += kThreads) c4[q] = make_uint4(0u, 0u, 0u, 0u);
+        for (uint64_t c = lo + 4 * quads + tid; c < hi; c += kThreads) a.conteos[c] = 0u;
+    }
     const bool complete = wait_all(hdr, passed, &s_red[0]);
 
     // ---- phase 2: this CTA's bucket (none after a wait that gave up: the
