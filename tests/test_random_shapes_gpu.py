@@ -58,3 +58,46 @@ def test_random_shape(ug, oracle_lib, seed):
     got = gpu_build(ug, rows, dims, origin, cs, ug.GRID_STABLE if stable else 0, params=p)
     ref = oracle_lib.build(rows, dims, origin, cs, order=order)
     assert_matches_oracle(oracle_lib, rows, got, ref, stable)
+
+
+@pytest.mark.parametrize("seed", range(0, CASES, 4))
+def test_random_shape_phase_by_phase(ug, oracle_lib, seed):
+    """The pages' chain one entry point at a time (clear, count, scan,
+    scatter in both modes, reorder) on the same random shapes."""
+    o = oracle_lib
+    n, dims, origin, cs, rows, _, order = _case(seed)
+    C = dims[0] * dims[1] * dims[2]
+    p = ug.make_params(n, dims, origin, cs, order=order)
+    ref = o.build(rows, dims, origin, cs, order=order)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).cuda()  # noqa: E731
+    u32 = lambda t: t.cpu().numpy().view(np.uint32)  # noqa: E731
+    origen = torch.from_numpy(rows).cuda()
+    ws = torch.zeros(ug.grid_workspace_bytes(p, ug.GRID_STABLE), dtype=torch.uint8, device="cuda")
+
+    conteos = torch.full((C,), 5, dtype=torch.int32, device="cuda")
+    celda = torch.empty(n, dtype=torch.int32, device="cuda")
+    ug.grid_clear(conteos, p)
+    ug.grid_count(origen, conteos, celda, p)
+    assert np.array_equal(u32(celda), ref["celdaDe"])
+    assert np.array_equal(u32(conteos), ref["conteos"])
+
+    inicios = torch.empty(C + 1, dtype=torch.int32, device="cuda")
+    ug.grid_scan(conteos, inicios, ws, p)
+    assert ug.grid_status(ws) == 0
+    assert np.array_equal(u32(inicios), ref["inicios"])
+
+    cursor = torch.zeros(C, dtype=torch.int32, device="cuda")
+    ordenado = torch.empty(n, dtype=torch.int32, device="cuda")
+    ug.grid_scatter(celda, inicios, cursor, ordenado, ws, p)
+    assert ug.grid_status(ws) == 0
+    assert np.array_equal(u32(cursor), ref["conteos"])
+    assert np.array_equal(o.canonicalise(ref["inicios"], u32(ordenado)), ref["ordenado"])
+    cursor.zero_()
+    ug.grid_scatter(celda, inicios, cursor, ordenado, ws, p, flags=ug.GRID_STABLE)
+    assert ug.grid_status(ws) == 0
+    assert np.array_equal(u32(ordenado), ref["ordenado"])
+
+    destino = torch.empty_like(origen)
+    ug.grid_reorder(ordenado, origen, destino, ws, p)
+    assert ug.grid_status(ws) == 0
+    assert np.array_equal(destino.cpu().numpy().view(np.uint32), ref["destino"].view(np.uint32))
