@@ -18,7 +18,7 @@
 //            read once in order and written once, so no gather pass is
 //            needed ("Reordenar por celda…", §El kernel de reordenación:
 //            destino[k] = origen[ordenado[k]] holds by construction)
-// The order within a cell is that of the atomics, so this build serves the
+// The order within a cell is that of the atomics, so the cluster build serves the
 // non-stable mode; stable builds of small scenes take the one-CTA build.
 #include <atomic>
 
