@@ -181,14 +181,18 @@ int grid_reorder(const uint32_t *ordenado, const ugrid_particula *origen, ugrid_
 
 /* The whole build: what the pages' chain computes ("Construir el índice de
  * la rejilla…", §La cadena completa: clear conteos, count, scan, clear the
- * cursor, scatter, [segment sort], gather), in one cooperative launch.  The
- * particles are first sorted into buckets of consecutive cells with shared-
- * memory counters, then each bucket's cells are counted, scanned and placed by
- * one CTA (a two-level counting sort); a bucket too large for one CTA sends
- * the launch down an atomic-counter path, and grids of more than 8192 buckets
- * use that path from the start.  Where a cooperative launch is not available
- * the entry points above run one after the other, the second clear folded
- * into the scan.
+ * cursor, scatter, [segment sort], gather), in one launch.  The particles are
+ * first sorted into buckets of consecutive cells with shared-memory counters,
+ * then each bucket's cells are counted, scanned and placed by one CTA (a
+ * two-level counting sort in one cooperative launch); a bucket too large for
+ * one CTA sends the launch down an atomic-counter path, and grids of more than
+ * 8192 buckets use that path from the start.  Small scenes (at most 32,768
+ * particles on 131,072 cells without GRID_STABLE, 8,192 on 8,192 with it) run
+ * on one thread-block cluster or one CTA; sparse grids (at least four cells
+ * per particle, at most 1,024 particles per CTA) exchange the particles with
+ * one grid barrier.  Where a cooperative launch is not available the entry
+ * points above run one after the other, the second clear folded into the
+ * scan.
  * On return (once the stream has run) conteos holds the histogram, celdaDe the
  * cells, inicios the starts, ordenado the cell-grouped indices and destino
  * the reordered records; without GRID_STABLE the order inside a cell is
