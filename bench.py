@@ -13,8 +13,8 @@ Further passes in the same run:
                    per-kernel microseconds and the gather kernel's roofline;
   * end to end   — host buffers: pinned host origen -> device, build,
                    destino and inicios -> pinned host, all inside the events:
-                   steps in turn on two streams, each with its own device and
-                   host result arrays, over one timed region (`e2e`), and
+                   steps in turn on three streams, each with its own device
+                   and host result arrays, over one timed region (`e2e`), and
                    each step alone between its own events (`e2e_serial`);
   * neighbours   — the neighbour query on SPH-like scenes (20 and 50
                    particles per cell on 64^3 cells), in linear and Morton
@@ -672,20 +672,22 @@ def run_gpu(args) -> None:
     if not np.array_equal(host_inicios.numpy()[[0, cells]], np.array([0, n], dtype=np.int32)):
         raise RuntimeError("end-to-end result is inconsistent")
 
-    # ---- end to end, pipelined: two streams, each with its own device and
-    # host result arrays, so that one step's copies overlap the other's build
-    # (the copies in and out share the host link, the builds are hidden) ----
+    # ---- end to end, pipelined: --e2e-streams streams, each with its own
+    # device and host result arrays, so that one step's copy in overlaps
+    # another's copies out and the builds hide under the copies ----
     e2e_pipe = None
     if args.e2e_steps > 0:
-        pipe_streams = [stream, torch.cuda.Stream()]
-        pipe_bufs = [b, ug.GridBuffers.allocate(p, flags)]
-        pipe_in = [dev_in, torch.empty_like(origen)]
-        pipe_dest = [host_dest, torch.empty((n, 8), dtype=torch.float32).pin_memory()]
-        pipe_inicios = [host_inicios, torch.empty(cells + 1, dtype=torch.int32).pin_memory()]
+        ways = max(2, args.e2e_streams)
+        pipe_streams = [stream] + [torch.cuda.Stream() for _ in range(ways - 1)]
+        pipe_bufs = [b] + [ug.GridBuffers.allocate(p, flags) for _ in range(ways - 1)]
+        pipe_in = [dev_in] + [torch.empty_like(origen) for _ in range(ways - 1)]
+        pipe_dest = [host_dest] + [torch.empty((n, 8), dtype=torch.float32).pin_memory() for _ in range(ways - 1)]
+        pipe_inicios = [host_inicios] + [torch.empty(cells + 1, dtype=torch.int32).pin_memory()
+                                         for _ in range(ways - 1)]
 
         def pipelined(count):
             for k in range(count):
-                j = k & 1
+                j = k % ways
                 bj = pipe_bufs[j]
                 ug.grid_build_host(host_in, pipe_dest[j], pipe_inicios[j], pipe_in[j], bj.destino, bj.conteos,
                                    bj.celdaDe, bj.inicios, bj.ordenado, bj.ws, p, flags, pipe_streams[j])
@@ -695,26 +697,27 @@ def run_gpu(args) -> None:
         barrier(dist)
         settle(0)  # L2 flushed once, then the stream held while the host enqueues
         start = torch.cuda.Event(enable_timing=True)
-        ends = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(ways)]
         start.record(pipe_streams[0])
-        pipe_streams[1].wait_event(start)
+        for j in range(1, ways):
+            pipe_streams[j].wait_event(start)
         pipelined(args.e2e_steps)
-        for j in range(2):
+        for j in range(ways):
             ends[j].record(pipe_streams[j])
         torch.cuda.synchronize()
         pipe_ms = max(start.elapsed_time(e) for e in ends)
         for bj in pipe_bufs:
             if ug.grid_status(bj.ws) != 0:
                 raise RuntimeError("device status set during the pipelined end-to-end pass")
-        for j in range(2):
+        for j in range(min(ways, args.e2e_steps)):
             if not np.array_equal(pipe_inicios[j].numpy()[[0, cells]], np.array([0, n], dtype=np.int32)):
                 raise RuntimeError("pipelined end-to-end result is inconsistent")
         pipe_total = max_over_ranks(pipe_ms, dist)
         e2e_pipe = {"value": job_rate(world, n, pipe_total / args.e2e_steps), "unit": UNIT,
-                    "ms_per_step": pipe_total / args.e2e_steps, "steps": args.e2e_steps, "streams": 2,
+                    "ms_per_step": pipe_total / args.e2e_steps, "steps": args.e2e_steps, "streams": ways,
                     "h2d_bytes_per_step": int(host_in.numel() * 4),
                     "d2h_bytes_per_step": int(host_dest.numel() * 4 + host_inicios.numel() * 4),
-                    "note": "grid_build_host on two streams in turn, one timed region over all steps; "
+                    "note": f"grid_build_host on {ways} streams in turn, one timed region over all steps; "
                             "L2 flushed once before it"}
         del pipe_bufs, pipe_in, pipe_dest, pipe_inicios
 
@@ -763,8 +766,8 @@ def run_gpu(args) -> None:
         "next_rows_cold": next_rows,
         "phases_gbs_cold": {k: alg[k] / (phase_us[k] * 1e-6) / 1e9 for k in phase_names},
         "cpu_baseline": cpu,
-        # End to end through grid_build_host: frames in turn on two streams (the
-        # way a caller with a stream of scenes uses it), and each step alone.
+        # End to end through grid_build_host: scenes in turn on several streams
+        # (the way a caller with a stream of scenes uses it), and each step alone.
         "e2e": e2e_pipe if e2e_pipe is not None else e2e_serial,
         "e2e_serial": e2e_serial,
         "neighbour_query": neighbour,
@@ -793,6 +796,8 @@ def main(argv=None) -> None:
                     help="timed builds of each of the five workloads (0 skips that leg)")
     ap.add_argument("--phase-steps", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--e2e-streams", type=int, default=3,
+                    help="streams the end-to-end steps take in turn (at least 2)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time")
     ap.add_argument("--reference-budget", type=float, default=150.0,
                     help="seconds the --impl reference steps may take in all")
