@@ -85,8 +85,7 @@ build_cluster_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ desti
 #pragma unroll
     for (uint32_t k = 0; k < kItems; ++k) {
         const uint32_t i = p0 + k * kThreads + tid;
-        cell[k] = i < p1 ? cell_of(head[k], g) : 0u;
-        if (i < p1) celdaDe[i] = cell[k];
+        cell[k] = i < p1 ? cell_of(head[k], g) : 0u;  // celdaDe written at the end
     }
     cluster.barrier_wait();
 #pragma unroll
@@ -136,6 +135,12 @@ build_cluster_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ desti
             st[e] = start;
             start += c8[e];
         }
+        reinterpret_cast<uint4 *>(s_count)[2 * tid] = make_uint4(st[0], st[1], st[2], st[3]);
+        reinterpret_cast<uint4 *>(s_count)[2 * tid + 1] = make_uint4(st[4], st[5], st[6], st[7]);
+        // Every slice's starts in place: the arrival releases them; conteos
+        // and inicios are stored while the barrier completes (a release
+        // waits for the stores before it, so they come after).
+        cluster.barrier_arrive();
         const uint32_t lo = rank * slice, hi = min(cells, lo + slice);  // this slice's cells
         const uint32_t c0 = lo + 8u * tid;
         if (8u * tid < slice && c0 + 8 <= hi) {
@@ -153,10 +158,8 @@ build_cluster_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ desti
             }
         }
         if (rank == ctas - 1 && tid == 0) inicios[cells] = n;
-        reinterpret_cast<uint4 *>(s_count)[2 * tid] = make_uint4(st[0], st[1], st[2], st[3]);
-        reinterpret_cast<uint4 *>(s_count)[2 * tid + 1] = make_uint4(st[4], st[5], st[6], st[7]);
     }
-    cluster.sync();  // every slice's starts in place
+    cluster.barrier_wait();
 
     // scatter: each particle to its position, with its record.  The starts
     // are read from the owners' slices first; the closing barrier (no CTA
@@ -179,6 +182,7 @@ build_cluster_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ desti
     for (uint32_t k = 0; k < kItems; ++k) {
         const uint32_t i = p0 + k * kThreads + tid;
         if (i < p1) {
+            celdaDe[i] = cell[k];
             ordenado[pos[k]] = i;
             store_cs(destino + 2 * (uint64_t)pos[k], head[k]);
             store_cs(destino + 2 * (uint64_t)pos[k] + 1, tail[k]);
