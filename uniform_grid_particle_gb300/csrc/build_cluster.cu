@@ -166,18 +166,24 @@ build_cluster_kernel(const uint4 *__restrict__ origen, uint4 *__restrict__ desti
     // leaves while another may still read its slice) completes during the
     // stores.
     uint32_t pos[kItems];
-    uint4 tail[kItems];
 #pragma unroll
     for (uint32_t k = 0; k < kItems; ++k) {
         const uint32_t i = p0 + k * kThreads + tid;
         if (i < p1) {
             const uint32_t owner = cell[k] / slice;
             pos[k] = *(cluster.map_shared_rank(s_count, (int)owner) + (cell[k] - owner * slice)) + slot[k];
-            tail[k] = load_nc_na(origen + 2 * (uint64_t)i + 1);
         }
     }
-    // The arrival releases: the remote loads above are performed before it.
+    // The arrival releases: the remote loads above are performed before it
+    // (the records' second halves are loaded after it, so that it does not
+    // wait for them too).
     cluster.barrier_arrive();
+    uint4 tail[kItems];
+#pragma unroll
+    for (uint32_t k = 0; k < kItems; ++k) {
+        const uint32_t i = p0 + k * kThreads + tid;
+        if (i < p1) tail[k] = load_nc_na(origen + 2 * (uint64_t)i + 1);
+    }
 #pragma unroll
     for (uint32_t k = 0; k < kItems; ++k) {
         const uint32_t i = p0 + k * kThreads + tid;
