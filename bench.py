@@ -284,13 +284,28 @@ STABLE_KERNEL = ("build_bucketed_kernel<true>", None)
 TRAFFIC_SCENE = "headline"
 
 
+def build_kernel(n: int, cells: int, stable: bool, sms: int) -> str:
+    """The kernel grid_build launches for a scene of n particles on `cells`
+    cells: the plan limits of the library's grid_build (cluster, one-CTA,
+    sparse, bucketed), restated to label the timed launch."""
+    mode = "true" if stable else "false"
+    if n and not stable and n <= 32768 and cells <= 131072:
+        return "build_cluster_kernel"
+    if n and n <= 8192 and cells <= 8192:
+        return f"build_small_kernel<{mode}>"
+    if n and 4 * n <= cells and n <= 2 * sms * 1024:
+        return f"build_sparse_kernel<{mode}>"
+    return f"build_bucketed_kernel<{mode}>"
+
+
 def roofline_entry(flags: int, total_alg: int, ms_per_step: float, peak: float, peak_kind: str,
-                   scene_name: str = TRAFFIC_SCENE) -> dict:
+                   scene_name: str = TRAFFIC_SCENE, kernel: str | None = None) -> dict:
     """The timed step is one launch of the build kernel: its algorithmic
     bytes are the whole build's, its duration the step's event time."""
     achieved = total_alg / (ms_per_step * 1e-3) / 1e9
-    kernel, sources = BUILD_KERNEL if flags == 0 else STABLE_KERNEL
-    if scene_name != TRAFFIC_SCENE:
+    default_kernel, sources = BUILD_KERNEL if flags == 0 else STABLE_KERNEL
+    kernel = kernel or default_kernel
+    if scene_name != TRAFFIC_SCENE or kernel != default_kernel:
         sources = None
     return {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
             "unit": "GB/s", "frac": achieved / peak, "algorithmic_bytes_per_launch": total_alg,
@@ -298,15 +313,15 @@ def roofline_entry(flags: int, total_alg: int, ms_per_step: float, peak: float, 
             "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
 
 
-def workload_config(scene, args) -> dict:
+def workload_config(scene, args, kernel: str | None = None) -> dict:
     return {
         "workload": (f"{scene.name}: N={scene.n:,} particles, grid {scene.dims[0]}x{scene.dims[1]}x{scene.dims[2]}"
                      f" over [-5,5)^3, 32-byte Particula AoS, {scene.kind} positions"),
         "build": ("stable (ordenado ordered by particle index inside each cell)" if args.stable
                   else "atomic (order inside a cell unspecified)"),
         "l2": "flushed between steps (a 2x L2 buffer is written outside the timed events)",
-        "launch": ("grid_build on a stream (C ABI): one cooperative launch of "
-                   + (STABLE_KERNEL[0] if args.stable else BUILD_KERNEL[0])),
+        "launch": ("grid_build on a stream (C ABI): one launch of "
+                   + (kernel or (STABLE_KERNEL[0] if args.stable else BUILD_KERNEL[0]))),
     }
 
 
@@ -316,7 +331,8 @@ def workload_config(scene, args) -> dict:
 CONFIG_SCENES = ["tiny", "scan_dominated", "headline", "contention", "stress"]
 
 
-def time_configs(ug, scenes, flags: int, steps: int, warmup: int, timed, settle, stream, peak: float) -> dict:
+def time_configs(ug, scenes, flags: int, steps: int, warmup: int, timed, settle, stream, peak: float,
+                 sms: int) -> dict:
     """Per workload: mean and median microseconds per build, Mparticles/s,
     algorithmic GB/s and the fraction of the HBM peak.  The stress workload
     runs its ten ping-pong builds (each reads the previous build's destino)
@@ -347,7 +363,7 @@ def time_configs(ug, scenes, flags: int, steps: int, warmup: int, timed, settle,
             return {"us_mean": mean, "us_median": statistics.median(us), "mparticles_per_s": n / mean,
                     "achieved_gbs": gbs, "frac": gbs / peak, "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
 
-        entry = {"n": n, "cells": cells, "algorithmic_bytes": alg}
+        entry = {"n": n, "cells": cells, "algorithmic_bytes": alg, "kernel": build_kernel(n, cells, bool(flags), sms)}
         if scene.builds > 1:
             pong = ug.GridBuffers.allocate(p, flags)
             first, rest = [], []
@@ -474,6 +490,7 @@ def run_gpu(args) -> None:
     origen = torch.from_numpy(rows).cuda()
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    step_kernel = build_kernel(n, cells, bool(flags), torch.cuda.get_device_properties(local).multi_processor_count)
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device="cuda")
     sleep = getattr(torch.cuda, "_sleep", None)
 
@@ -731,7 +748,8 @@ def run_gpu(args) -> None:
     # ---- every workload, whole builds, L2 flushed before each ----
     configs = None
     if args.config_steps > 0:
-        configs = time_configs(ug, scenes, flags, args.config_steps, args.warmup, timed, settle, stream, peak)
+        configs = time_configs(ug, scenes, flags, args.config_steps, args.warmup, timed, settle, stream, peak,
+                               torch.cuda.get_device_properties(local).multi_processor_count)
 
     if rank != 0:
         if dist is not None:
@@ -745,8 +763,8 @@ def run_gpu(args) -> None:
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
-        "config": workload_config(scene, args),
-        "roofline": roofline_entry(flags, total_alg, ms_per_step, peak, peak_kind, scene.name),
+        "config": workload_config(scene, args, step_kernel),
+        "roofline": roofline_entry(flags, total_alg, ms_per_step, peak, peak_kind, scene.name, step_kernel),
         "gather_roofline": {"kernel": "reorder_kernel (grid_reorder alone, L2 flushed before it)",
                             "achieved": gather_gbs, "peak": peak, "unit": "GB/s", "frac": gather_gbs / peak,
                             "algorithmic_bytes_per_launch": alg["gather"],
