@@ -169,6 +169,12 @@ cudaError_t launch_build_cluster(const ugrid_particula *origen, ugrid_particula 
 
 // The whole build in one CTA, for scenes of at most kSmallMaxParticles
 // particles on at most kSmallMaxCells cells (see build_small.cu).
+constexpr uint32_t kSmallMaxParticles = 8192;
+constexpr uint32_t kSmallMaxCells = 8192;
+cudaError_t launch_build_small(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
+                               uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, uint32_t n,
+                               uint32_t cells, const Geometry &g, bool stable, cudaStream_t s);
+
 // The sparse build: at most this many particles per CTA of its launch
 // (measured: with more, its plain-load gather and its phase 1 make it slower
 // than the bucketed build).
@@ -176,12 +182,6 @@ constexpr uint32_t kSparseMaxParticlesPerCta = 1024;
 // grid_build takes the sparse build when there are at least this many cells
 // per particle.
 constexpr uint64_t kSparseCellsPerParticle = 4;
-constexpr uint32_t kSmallMaxParticles = 8192;
-constexpr uint32_t kSmallMaxCells = 8192;
-cudaError_t launch_build_small(const ugrid_particula *origen, ugrid_particula *destino, uint32_t *conteos,
-                               uint32_t *celdaDe, uint32_t *inicios, uint32_t *ordenado, uint32_t n,
-                               uint32_t cells, const Geometry &g, bool stable, cudaStream_t s);
-
 // The build for sparse grids, one cooperative launch with one grid barrier
 // (see build_sparse.cu).  Its table of per-CTA bucket offsets lives in the
 // fused build's counter array `counts` (the kernel marks it not clean).
