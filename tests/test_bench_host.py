@@ -31,3 +31,32 @@ def test_pair_tests_counts_the_27_cells():
                                  if 0 <= X < gx and 0 <= Y < gy and 0 <= Z < gz)
                     want += int(c[x + gx * (y + gy * z)]) * around
         assert bench.pair_tests(c, dims) == want, dims
+
+
+def test_build_kernel_labels_follow_the_library_limits():
+    """bench.py names the kernel a scene's build launches from the plan
+    limits of grid_build; those limits live in the library's internal header,
+    so a change there must show up here."""
+    import re
+
+    hdr = open(os.path.join(ROOT, "uniform_grid_particle_gb300", "csrc", "ugrid_internal.cuh")).read()
+
+    def const(name):
+        return int(re.search(rf"constexpr \w+ {name} = (\d+);", hdr).group(1))
+
+    bench = _bench()
+    cl_n, cl_c = const("kClusterMaxParticles"), const("kClusterMaxCells")
+    sm_n, sm_c = const("kSmallMaxParticles"), const("kSmallMaxCells")
+    per_cta, cells_per = const("kSparseMaxParticlesPerCta"), const("kSparseCellsPerParticle")
+    sms = 152
+    k = bench.build_kernel
+    assert k(cl_n, cl_c, False, sms) == "build_cluster_kernel"
+    assert k(cl_n + 1, cl_c, False, sms) != "build_cluster_kernel"
+    assert k(cl_n, cl_c + 1, False, sms) != "build_cluster_kernel"
+    assert k(sm_n, sm_c, True, sms) == "build_small_kernel<true>"
+    assert k(sm_n + 1, sm_c, True, sms) != "build_small_kernel<true>"
+    n = 2 * sms * per_cta
+    assert k(n, cells_per * n, False, sms) == "build_sparse_kernel<false>"
+    assert k(n + 1, cells_per * (n + 1), False, sms) == "build_bucketed_kernel<false>"
+    assert k(n, cells_per * n - 1, True, sms) == "build_bucketed_kernel<true>"
+    assert k(1_000_000, 128 ** 3, False, sms) == "build_bucketed_kernel<false>"
