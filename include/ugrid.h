@@ -111,7 +111,10 @@ typedef struct grid_ws_header {
     uint32_t bar_exit;     /* CTAs that finished the running single-launch build; 0 between calls */
     uint32_t counts_clean; /* cells of the fused build's counter array known to be zero */
     uint32_t buckets_clean; /* 1 when the bucketed build's per-bucket totals are all zero */
-    uint32_t reserved0[24]; /* the words above fill the first 128 bytes */
+    uint32_t bar_extra;    /* added to every grid barrier's arrival target: 0 in use (a
+                            * workspace is zero-filled); a test sets it so that the
+                            * barriers' bounded waits run out */
+    uint32_t reserved0[23]; /* the words above fill the first 128 bytes */
     uint32_t bar_count;    /* grid-barrier arrivals of the running single-launch build; 0 between
                             * calls.  Alone in its 128-byte line: every CTA polls it. */
     uint32_t reserved[31];

@@ -1,9 +1,10 @@
 """Device-detected problems come back as status codes and leave the GPU usable.
 
-No test here faults, traps or hangs the GPU: the wait that runs out is the
-scan's look-back on a tile that no CTA was given (its one-second limit ends
-it), and the out-of-range indices are caught by the kernels' own bounds
-checks before any access.
+No test here faults, traps or hangs the GPU: the waits that run out are the
+scan's look-back on a tile that no CTA was given and the single-launch
+builds' grid barriers with their target raised past the CTA count (each
+wait's one-second limit ends it), and the out-of-range indices are caught by
+the kernels' own bounds checks before any access.
 """
 import numpy as np
 import pytest
@@ -102,3 +103,52 @@ def test_gpu_still_usable_after_faults(ug, oracle_lib):
     b.build(torch.from_numpy(rows).cuda(), p)
     assert ug.grid_status(b.ws) == 0
     assert np.array_equal(to_u32(b.inicios), oracle_lib.build(rows, s.dims, s.origin, s.cell_size)["inicios"])
+
+
+# A grid barrier's arrival target is raised by the header's bar_extra word
+# (word 8).  With it set every CTA still arrives, so all data is written
+# before anyone reads it, but no wait ever sees its target: each runs out
+# after its one-second limit and the build reports the timeout.  The last
+# CTA to leave still resets the barrier words, and the next build with the
+# word back at zero is exact.
+BAR_EXIT, BAR_EXTRA, BAR_COUNT = 5, 8, 32
+BARRIER_SCENES = [
+    # (particles, sides, flags): the plan grid_build picks for each
+    (40_000, (64, 64, 64), 0),              # sparse: one grid barrier
+    (40_000, (64, 64, 64), 1),              # sparse, stable
+    (40_000, (16, 16, 16), 0),              # bucketed: two grid barriers
+    (40_000, (16, 16, 16), 1),              # bucketed, stable
+    (400_000, (512, 512, 257), 0),          # more than 8192 buckets: the fused build
+]
+
+
+@pytest.mark.parametrize("n,dims,flags", BARRIER_SCENES)
+def test_grid_barrier_waits_time_out_and_workspace_recovers(ug, oracle_lib, n, dims, flags):
+    from gpu_helpers import assert_matches_oracle
+
+    cs = np.float32(0.25)
+    rng = np.random.default_rng(n + dims[0] + flags)
+    rows = np.zeros((n, 8), np.float32)
+    rows[:, :3] = (rng.random((n, 3)) * np.array(dims) * float(cs)).astype(np.float32)
+    rows[:, 3:] = rng.random((n, 5)).astype(np.float32)
+    p = ug.make_params(n, dims, (0, 0, 0), cs)
+    b = ug.GridBuffers.allocate(p, flags)
+    origen = torch.from_numpy(rows).cuda()
+    words = b.ws.view(torch.int32)
+    words[BAR_EXTRA] = 1
+    b.build(origen, p, flags)
+    assert ug.grid_status(b.ws) == ETIMEOUT
+    header = words[:64].cpu().numpy()
+    assert header[BAR_COUNT] == 0 and header[BAR_EXIT] == 0, "the last CTA reset the barrier words"
+    words[BAR_EXTRA] = 0
+    b.build(origen, p, flags)
+    got = {
+        "status": ug.grid_status(b.ws),
+        "conteos": to_u32(b.conteos),
+        "celdaDe": to_u32(b.celdaDe),
+        "inicios": to_u32(b.inicios),
+        "ordenado": to_u32(b.ordenado),
+        "destino": b.destino.cpu().numpy(),
+    }
+    ref = oracle_lib.build(rows, dims, (0, 0, 0), cs)
+    assert_matches_oracle(oracle_lib, rows, got, ref, bool(flags))

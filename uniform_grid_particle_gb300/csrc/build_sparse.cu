@@ -135,7 +135,7 @@ __device__ __forceinline__ uint32_t source_of(const uint32_t *s_off, uint32_t so
 // timeout is recorded in the status word).
 __device__ __forceinline__ bool wait_all(grid_ws_header *hdr, uint32_t passed, uint32_t *s_flag) {
     if (threadIdx.x == 0) {
-        const uint32_t target = passed * gridDim.x;
+        const uint32_t target = passed * gridDim.x + *reinterpret_cast<volatile uint32_t *>(&hdr->bar_extra);
         uint32_t ok = 1u;
         if (fused::load_acquire(&hdr->bar_count) < target) {
             const unsigned long long start = global_ns();

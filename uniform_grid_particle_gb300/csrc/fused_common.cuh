@@ -59,7 +59,7 @@ __device__ __forceinline__ void grid_arrive(grid_ws_header *hdr, uint32_t &passe
 
 __device__ inline void grid_wait(grid_ws_header *hdr, uint32_t passed) {
     if (threadIdx.x == 0) {
-        const uint32_t target = passed * gridDim.x;
+        const uint32_t target = passed * gridDim.x + *reinterpret_cast<volatile uint32_t *>(&hdr->bar_extra);
         if (load_acquire(&hdr->bar_count) < target) {
             const unsigned long long start = global_ns();
             uint32_t polls = 0;
