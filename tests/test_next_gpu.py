@@ -69,6 +69,36 @@ def test_reorder_many_matches_oracle(ug, oracle_lib):
     assert np.array_equal(dsts[0].cpu().numpy().view(np.uint32), got["destino"].view(np.uint32))
 
 
+# Record widths (in u32 words) of each call: the TMA form serves records of
+# at most 64 bytes (128-byte slots up to 32 bytes, 256-byte slots above), the
+# plain kernel wider ones.
+MANY_CASES = [
+    (1, [4]), (3, [4, 4]), (5, [8, 4]), (127, [4, 12]), (128, [16]), (129, [4, 4, 4, 4]),
+    (4099, [12, 16]), (100_003, [4, 4]), (100_003, [8, 16, 12]), (65_536, [20, 4]),
+    (20_001, [64]), (300_000, [4, 8]),
+]
+
+
+@pytest.mark.parametrize("n,widths", MANY_CASES)
+def test_reorder_many_shapes(ug, oracle_lib, n, widths):
+    rng = np.random.default_rng(n + len(widths))
+    # Random stretches and stretches already in order, so that chunks take
+    # both the gathered and the plain-load paths.
+    ordenado = rng.permutation(n).astype(np.uint32)
+    for lo in range(0, n, 4096):
+        if rng.random() < 0.3:
+            ordenado[lo:lo + 1000] = np.sort(ordenado[lo:lo + 1000])
+    hosts = [rng.integers(0, 2**32, (n, w), dtype=np.uint64).astype(np.uint32) for w in widths]
+    srcs = [torch.from_numpy(h).cuda() for h in hosts]
+    dsts = [torch.full_like(t, 0x7f7f7f7f) for t in srcs]
+    p = ug.make_params(n, (8, 8, 8), (0, 0, 0), 1.0)
+    ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
+    ug.grid_reorder_many(torch.from_numpy(ordenado.view(np.int32)).cuda(), list(zip(srcs, dsts)), ws, p)
+    assert ug.grid_status(ws) == 0
+    for h, d in zip(hosts, dsts):
+        assert np.array_equal(d.cpu().numpy(), oracle_lib.reorder_records(ordenado, h))
+
+
 def test_reorder_many_rejects_index_out_of_range(ug):
     n = 2000
     p = ug.make_params(n, (4, 4, 4), (0, 0, 0), 1.0)

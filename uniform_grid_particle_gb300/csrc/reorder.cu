@@ -183,18 +183,23 @@ cudaError_t reorder_grid(int *ctas) {
 
 }  // namespace
 
-cudaError_t record_tensor_map(const ugrid_particula *origen, uint32_t n, CUtensorMap *map) {
+cudaError_t rows_tensor_map(const void *base, uint32_t row_bytes, uint32_t rows, CUtensorMap *map) {
+    if (row_bytes == 0 || row_bytes % 16 || row_bytes > 1024) return cudaErrorInvalidValue;
     const EncodeTiled encode = encode_tiled();
     if (encode == nullptr) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {8, n};
-    const cuuint64_t strides[1] = {sizeof(ugrid_particula)};
-    const cuuint32_t box[2] = {8, 1};
+    const cuuint64_t dims[2] = {row_bytes / 4, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {row_bytes / 4, 1};
     const cuuint32_t elem_strides[2] = {1, 1};
-    if (encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<ugrid_particula *>(origen), dims, strides, box,
+    if (encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides, box,
                elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     return cudaSuccess;
+}
+
+cudaError_t record_tensor_map(const ugrid_particula *origen, uint32_t n, CUtensorMap *map) {
+    return rows_tensor_map(origen, (uint32_t)sizeof(ugrid_particula), n, map);
 }
 
 cudaError_t launch_reorder(const uint32_t *ordenado, const ugrid_particula *origen,

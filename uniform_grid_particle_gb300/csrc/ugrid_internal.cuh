@@ -133,6 +133,9 @@ cudaError_t launch_scatter(const uint32_t *celdaDe, const uint32_t *inicios, uin
 // origen described to the tensor memory accelerator as n rows of eight u32
 // words, with a box of one whole row (the form a tile::gather4 copy reads).
 cudaError_t record_tensor_map(const ugrid_particula *origen, uint32_t n, CUtensorMap *map);
+// The same for any array of `rows` rows of row_bytes bytes (a multiple of 16,
+// at most 1024), read as u32 words.
+cudaError_t rows_tensor_map(const void *base, uint32_t row_bytes, uint32_t rows, CUtensorMap *map);
 
 cudaError_t launch_reorder(const uint32_t *ordenado, const ugrid_particula *origen,
                            ugrid_particula *destino, uint32_t n, uint32_t *status, cudaStream_t s,
