@@ -111,6 +111,17 @@ constexpr size_t tma_smem_bytes(uint32_t slot) {
            (size_t)kTmaWarps * kTmaStages * (sizeof(unsigned long long) + sizeof(uint32_t));
 }
 
+// The record position of 16-byte piece h when a record has `pieces` pieces
+// (1 to 4 in the TMA form): a shift or a multiply, not a division.
+__device__ __forceinline__ uint32_t position_of(uint32_t h, uint32_t pieces) {
+    switch (pieces) {
+        case 1: return h;
+        case 2: return h >> 1;
+        case 3: return h / 3u;
+        default: return h >> 2;
+    }
+}
+
 __global__ void __launch_bounds__(32 * kTmaWarps)
 reorder_many_tma_kernel(const __grid_constant__ ManyMaps m, const uint32_t *__restrict__ ordenado, uint32_t n,
                         uint32_t *status) {
@@ -134,45 +145,57 @@ reorder_many_tma_kernel(const __grid_constant__ ManyMaps m, const uint32_t *__re
     const uint32_t chunks = (uint32_t)(((uint64_t)n + kChunk - 1) / kChunk);
     const uint32_t first = blockIdx.x * kTmaWarps + warp, stride = gridDim.x * kTmaWarps;
     const uint32_t mine = first < chunks ? (chunks - 1u - first) / stride + 1u : 0u;
-    const uint32_t items = mine * m.count;  // item i: chunk i / count of this warp, array i % count
+    const uint32_t items = mine * m.count;  // item i: this warp's chunk i / count, array i % count
 
+    // The item to issue next, and the lane's rows of its chunk: the arrays of
+    // one chunk are issued one after another and share the rows.
+    uint32_t iss_chunk = 0, iss_array = 0;
+    int row[4] = {0, 0, 0, 0};
+    uint32_t v = 0, lanes = 0;
+    bool copy_plain = true;
     auto issue = [&](uint32_t i) {
-        const uint32_t s = i % kTmaStages, a = i % m.count;
-        const uint64_t k0 = (uint64_t)(first + (i / m.count) * stride) * kChunk + 4u * lane;
-        const uint32_t v = k0 < n ? (uint32_t)min((uint64_t)4, n - k0) : 0u;
-        int row[4] = {0, 0, 0, 0};
-        bool lane_bad = false;
-        if (v > 0) {
+        const uint32_t s = i % kTmaStages, a = iss_array;
+        const uint64_t k0 = (uint64_t)(first + iss_chunk * stride) * kChunk + 4u * lane;
+        if (a == 0) {
+            v = k0 < n ? (uint32_t)min((uint64_t)4, n - k0) : 0u;
+            bool lane_bad = false;
+            if (v > 0) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t r = __ldg(ordenado + k0 + min((uint32_t)e, v - 1u));
-                lane_bad |= r >= n;
-                row[e] = (int)r;
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t r = __ldg(ordenado + k0 + min((uint32_t)e, v - 1u));
+                    lane_bad |= r >= n;
+                    row[e] = (int)r;
+                }
             }
+            const bool chunk_bad = __any_sync(0xffffffffu, lane_bad);
+            lanes = __popc(__ballot_sync(0xffffffffu, v > 0));
+            if (lane_bad) record_status(status, kStatusBounds);
+            copy_plain = chunk_bad || rows_span(row, v) < kClusterRows;
         }
-        const bool chunk_bad = __any_sync(0xffffffffu, lane_bad);
-        const uint32_t lanes = __popc(__ballot_sync(0xffffffffu, v > 0));
-        if (lane_bad) record_status(status, kStatusBounds);
-        const bool near = !chunk_bad && rows_span(row, v) < kClusterRows;
         if (lane == 0) {
-            plain[s] = chunk_bad || near ? 1u : 0u;
-            mbar_arrive_expect(smem_addr(bar + s), chunk_bad || near ? 0u : lanes * 4u * m.bytes[a]);
+            plain[s] = copy_plain ? 1u : 0u;
+            mbar_arrive_expect(smem_addr(bar + s), copy_plain ? 0u : lanes * 4u * m.bytes[a]);
         }
         __syncwarp();
-        if (!chunk_bad && !near && v > 0)
+        if (!copy_plain && v > 0)
             gather4_records(smem_addr(stage + s * stage_bytes + lane * m.slot), &m.map[a], row, smem_addr(bar + s));
+        if (++iss_array == m.count) {
+            iss_array = 0;
+            ++iss_chunk;
+        }
     };
 
     for (uint32_t i = 0; i < min(items, (uint32_t)kTmaStages); ++i) issue(i);
+    uint32_t chunk = 0, a = 0;  // the item being written out
     for (uint32_t i = 0; i < items; ++i) {
-        const uint32_t s = i % kTmaStages, a = i % m.count;
+        const uint32_t s = i % kTmaStages;
         if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(bar + s), (i / kTmaStages) & 1u))) {  // the warp agrees
             if (lane == 0) record_status(status, kStatusTimeout);
             for (uint32_t j = i + 1; j < min(items, i + kTmaStages); ++j)
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(bar + j % kTmaStages), (j / kTmaStages) & 1u))) break;
             break;
         }
-        const uint64_t k0 = (uint64_t)(first + (i / m.count) * stride) * kChunk;
+        const uint64_t k0 = (uint64_t)(first + chunk * stride) * kChunk;
         const uint32_t rows = (uint32_t)min((uint64_t)kChunk, n - k0);
         const uint32_t pieces = m.bytes[a] / 16u, total = rows * pieces;
         uint4 *dst = m.dst[a] + k0 * pieces;
@@ -186,7 +209,7 @@ reorder_many_tma_kernel(const __grid_constant__ ManyMaps m, const uint32_t *__re
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t h = h0 + (uint32_t)k * 32u + lane;
-                    const uint32_t p = h / pieces;
+                    const uint32_t p = position_of(h, pieces);
                     from[k] = h < total ? __ldg(ordenado + k0 + p) : n;
                     if (from[k] < n) r4[k] = load_nc_na(src + (uint64_t)from[k] * pieces + (h - p * pieces));
                 }
@@ -199,10 +222,10 @@ reorder_many_tma_kernel(const __grid_constant__ ManyMaps m, const uint32_t *__re
             // piece per lane and store, 32 consecutive pieces per warp store.
             const unsigned char *st = stage + s * stage_bytes;
             for (uint32_t h = lane; h < total; h += 32u) {
-                const uint32_t p = h / pieces;
-                const uint4 v = *reinterpret_cast<const uint4 *>(st + (p >> 2) * m.slot + (p & 3u) * m.bytes[a] +
-                                                                 (h - p * pieces) * 16u);
-                store_cs(dst + h, v);
+                const uint32_t p = position_of(h, pieces);
+                const uint4 val = *reinterpret_cast<const uint4 *>(st + (p >> 2) * m.slot + (p & 3u) * m.bytes[a] +
+                                                                   (h - p * pieces) * 16u);
+                store_cs(dst + h, val);
             }
         }
         if (i + kTmaStages < items) {
@@ -210,6 +233,10 @@ reorder_many_tma_kernel(const __grid_constant__ ManyMaps m, const uint32_t *__re
             __syncwarp();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(i + kTmaStages);
+        }
+        if (++a == m.count) {
+            a = 0;
+            ++chunk;
         }
     }
     __syncwarp();
