@@ -99,6 +99,47 @@ def test_reorder_many_shapes(ug, oracle_lib, n, widths):
         assert np.array_equal(d.cpu().numpy(), oracle_lib.reorder_records(ordenado, h))
 
 
+@pytest.mark.parametrize("widths", [[12, 16], [4, 4, 4]])
+def test_reorder_many_bad_index_in_gathered_chunks(ug, oracle_lib, widths):
+    """Out-of-range indices inside chunks that would otherwise be gathered by
+    TMA (random order), in arrays of 48/64 and of 16 bytes: those chunks are
+    copied with plain loads, the bad records skipped, the rest exact."""
+    n = 70_001
+    rng = np.random.default_rng(31)
+    ordenado = rng.permutation(n).astype(np.uint32)
+    bad = np.array([0, 4097, 33_333, n - 1])
+    ordenado[bad] = n + np.arange(bad.size, dtype=np.uint32)
+    hosts = [rng.integers(0, 2**32, (n, w), dtype=np.uint64).astype(np.uint32) for w in widths]
+    srcs = [torch.from_numpy(h).cuda() for h in hosts]
+    dsts = [torch.zeros_like(t) for t in srcs]
+    p = ug.make_params(n, (8, 8, 8), (0, 0, 0), 1.0)
+    ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
+    ug.grid_reorder_many(torch.from_numpy(ordenado.view(np.int32)).cuda(), list(zip(srcs, dsts)), ws, p)
+    assert ug.grid_status(ws) == 4
+    ok = np.ones(n, bool)
+    ok[bad] = False
+    for h, d in zip(hosts, dsts):
+        got = d.cpu().numpy()
+        assert (got[bad] == 0).all(), "bad records are not written"
+        assert np.array_equal(got[ok], oracle_lib.reorder_records(ordenado[ok], h))
+
+
+def test_reorder_many_identity_order(ug, oracle_lib):
+    """An ordenado already in order: every chunk takes the plain-load copy."""
+    n = 123_457
+    rng = np.random.default_rng(32)
+    ordenado = np.arange(n, dtype=np.uint32)
+    hosts = [rng.integers(0, 2**32, (n, w), dtype=np.uint64).astype(np.uint32) for w in (4, 12)]
+    srcs = [torch.from_numpy(h).cuda() for h in hosts]
+    dsts = [torch.zeros_like(t) for t in srcs]
+    p = ug.make_params(n, (8, 8, 8), (0, 0, 0), 1.0)
+    ws = torch.zeros(ug.grid_workspace_bytes(p, 0), dtype=torch.uint8, device="cuda")
+    ug.grid_reorder_many(torch.from_numpy(ordenado.view(np.int32)).cuda(), list(zip(srcs, dsts)), ws, p)
+    assert ug.grid_status(ws) == 0
+    for h, d in zip(hosts, dsts):
+        assert np.array_equal(d.cpu().numpy(), oracle_lib.reorder_records(ordenado, h))
+
+
 def test_reorder_many_rejects_index_out_of_range(ug):
     n = 2000
     p = ug.make_params(n, (4, 4, 4), (0, 0, 0), 1.0)
