@@ -407,34 +407,52 @@ density_tile_kernel(const uint4 *__restrict__ parts, const uint32_t *__restrict_
         if (c == 0) s_first[r] = first;
     }
     __syncthreads();
-    if (tid == 0) {
-        uint32_t base = 0;
-        bool fits = true, mono = true;
-        uint32_t plane[3] = {0u, 0u, 0u};  // candidates of each z plane (saturating)
-        for (uint32_t r = 0; r < kStagedRows; ++r) {
-            const uint32_t size = s_start[r][nc];
-            // starts that decrease (inconsistent input) go to the walk, too
-            for (uint32_t c = 1; c <= nc; ++c) mono &= s_start[r][c] >= s_start[r][c - 1];
-            if (size > kStageMax || base + size > kStageMax) fits = false;
-            const uint32_t p = r / (kTileRows + 2);
-            plane[p] = plane[p] + size < plane[p] ? 0xffffffffu : plane[p] + size;
-            for (uint32_t c = 0; c <= nc; ++c) s_start[r][c] += base;
-            base += size;
+    static_assert(kStagedRows <= 32 && kTileRows * kTileCells <= 32, "warp 0 takes one row and one own cell per lane");
+    if (tid < 32) {
+        // Warp 0: lane r sums up staged row r, lane q counts the work items of
+        // own cell q (rows of own cells in order, cells in order in each).
+        const uint32_t lane = tid, w = x1 - x0, own = rows * w;
+        uint32_t size = 0, cnt = 0;
+        bool mono = true;  // starts that decrease (inconsistent input) go to the walk, too
+        if (lane < kStagedRows) {
+            size = s_start[lane][nc];
+            for (uint32_t c = 1; c <= nc; ++c) mono &= s_start[lane][c] >= s_start[lane][c - 1];
         }
-        fits &= mono;
-        s_total = fits ? base : 0xffffffffu;
-        s_sliced = !fits && mono && plane[0] <= kStageMax && plane[1] <= kStageMax && plane[2] <= kStageMax;
-        // One work item per two particles of an own cell (an odd last one alone).
-        uint32_t items = 0, q = 0;
-        for (uint32_t t = 0; t < rows; ++t) {
-            const uint32_t r = (kTileRows + 2) + 1 + t;
-            for (uint32_t c = x0 - xa; c < x1 - xa; ++c, ++q) {
-                s_items[q] = items;
-                items += (s_start[r][c + 1] - s_start[r][c] + 1) / 2;
+        if (lane < own) {
+            // One work item per two particles of an own cell (an odd last one alone).
+            const uint32_t t = lane / w, c = (x0 - xa) + (lane - t * w), r = (kTileRows + 2) + 1 + t;
+            cnt = (s_start[r][c + 1] - s_start[r][c] + 1) / 2;
+        }
+        uint32_t base = size, first_item = cnt;  // inclusive prefixes over the lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t b = __shfl_up_sync(0xffffffffu, base, o), i = __shfl_up_sync(0xffffffffu, first_item, o);
+            if (lane >= (uint32_t)o) {
+                base += b;
+                first_item += i;
             }
         }
-        s_items[q] = items;
-        if (items > kSliceRounds * kTileThreads) s_sliced = 0u;
+        const uint32_t staged = __shfl_sync(0xffffffffu, base, kStagedRows - 1);
+        const uint32_t items = __shfl_sync(0xffffffffu, first_item, 31);
+        base -= size;
+        first_item -= cnt;
+        const bool row_fits = lane >= kStagedRows || (size <= kStageMax && base + size <= kStageMax);
+        const bool all_mono = __all_sync(0xffffffffu, mono);
+        const bool fits = __all_sync(0xffffffffu, row_fits) && all_mono;
+        // Candidates of each z plane (kTileRows + 2 rows each), saturated at 2^32 - 1.
+        uint64_t plane[3] = {0u, 0u, 0u};
+#pragma unroll
+        for (uint32_t r = 0; r < kStagedRows; ++r) plane[r / (kTileRows + 2)] += __shfl_sync(0xffffffffu, size, r);
+        __syncwarp();  // every lane has read the starts before any is rebased
+        if (lane < kStagedRows)
+            for (uint32_t c = 0; c <= nc; ++c) s_start[lane][c] += base;
+        if (lane < own) s_items[lane] = first_item;
+        if (lane == 0) {
+            s_items[own] = items;
+            s_total = fits ? staged : 0xffffffffu;
+            s_sliced = !fits && all_mono && plane[0] <= kStageMax && plane[1] <= kStageMax &&
+                       plane[2] <= kStageMax && items <= kSliceRounds * kTileThreads;
+        }
     }
     __syncthreads();
     const uint32_t total = s_total;
