@@ -4,6 +4,7 @@ import ctypes
 import math
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -221,3 +222,22 @@ def test_build_host_checks_host_arrays(L):
     bad = list(dev)
     bad[0] = dev[0] + 8                                                 # misaligned device origen
     assert call(h, h + (1 << 24), h + (2 << 24), bad) == EINVAL
+
+
+def test_workspace_header_layout(tmp_path):
+    """The header words that the GPU fault tests write by index sit where the
+    tests expect them, as the C compiler lays the struct out: the status word
+    first, bar_exit at word 5, bar_extra at word 8, the barrier counter alone
+    at word 32, 256 bytes in all."""
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include "ugrid.h"\n'
+                   "int main(void) {\n"
+                   '  printf("%zu %zu %zu %zu %zu %zu\\n", offsetof(grid_ws_header, status),\n'
+                   "         offsetof(grid_ws_header, scan_ticket), offsetof(grid_ws_header, bar_exit),\n"
+                   "         offsetof(grid_ws_header, bar_extra), offsetof(grid_ws_header, bar_count),\n"
+                   "         sizeof(grid_ws_header));\n"
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", ugbuild.INCLUDE, str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert [int(v) for v in out] == [0, 4, 5 * 4, 8 * 4, 32 * 4, 256]
