@@ -265,6 +265,11 @@ def pin_canonicalise(o, seed: int = 9) -> None:
         rng.shuffle(seg)
     assert not np.array_equal(shuffled, stable)
     assert np.array_equal(o.canonicalise(inicios, shuffled), stable)
+    # Hand example with segments of every short length: empty, one, a reversed
+    # pair, three out of order, and a pair already in order.
+    inicios = np.array([0, 0, 1, 3, 6, 8], dtype=np.uint32)
+    ordenado = np.array([5, 9, 2, 7, 4, 1, 0, 3], dtype=np.uint32)
+    assert o.canonicalise(inicios, ordenado).tolist() == [5, 2, 9, 1, 4, 7, 0, 3]
 
 
 def pin_reorder_records(o, seed: int = 13) -> None:

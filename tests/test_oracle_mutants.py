@@ -54,6 +54,13 @@ MUTANTS = {
     "order_ignored_by_count": ("celdaDe[i] = cell_in_order(x, y, z, dims, order);",
                                "celdaDe[i] = cell_in_order(x, y, z, dims, 0u);"),
     "order_ignored_by_density": ("(uint32_t)z, dims, order);", "(uint32_t)z, dims, 0u);"),
+    "density_square_not_cube": ("sum += (double)pj[7] * t * t * t;", "sum += (double)pj[7] * t * t;"),
+    "density_x_one_sided": ("for (int dx = -1; dx <= 1; ++dx) {", "for (int dx = 0; dx <= 1; ++dx) {"),
+    "density_y_against_x": ("const double ey = (double)pj[1] - (double)pi[1];",
+                            "const double ey = (double)pj[1] - (double)pi[0];"),
+    "canonical_pairs_left_unsorted": ("if (b > a + 1u)", "if (b > a + 2u)"),
+    "records_fixed_stride": ("src + (uint64_t)record_bytes * ordenado[k], record_bytes);",
+                             "src + (uint64_t)32u * ordenado[k], record_bytes);"),
 }
 
 RUNNER = """
