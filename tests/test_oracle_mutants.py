@@ -54,6 +54,8 @@ MUTANTS = {
     "order_ignored_by_count": ("celdaDe[i] = cell_in_order(x, y, z, dims, order);",
                                "celdaDe[i] = cell_in_order(x, y, z, dims, 0u);"),
     "order_ignored_by_density": ("(uint32_t)z, dims, order);", "(uint32_t)z, dims, 0u);"),
+    "upper_clamp_strict": ("if ((double)f >= (double)dim)", "if ((double)f > (double)dim)"),
+    "below_clamped_to_top": ("    if (isnan(f) || f < 0.0f)\n        return 0u;", "    if (isnan(f) || f < 0.0f)\n        return dim - 1u;"),
     "density_square_not_cube": ("sum += (double)pj[7] * t * t * t;", "sum += (double)pj[7] * t * t;"),
     "density_x_one_sided": ("for (int dx = -1; dx <= 1; ++dx) {", "for (int dx = 0; dx <= 1; ++dx) {"),
     "density_y_against_x": ("const double ey = (double)pj[1] - (double)pi[1];",
