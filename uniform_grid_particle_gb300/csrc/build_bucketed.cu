@@ -536,13 +536,22 @@ build_bucketed_kernel(const __grid_constant__ CUtensorMap origen_map, BuildArgs 
             const uint32_t base = s_base;
             const uint32_t t = base <= a.n ? min(min(s_count, kBucketCap), a.n - base) : 0u;
             // (cell within the bucket) << 16 | slot within the cell; ~0u for none
+            static_assert(kBucketItems % 4 == 0, "pairs loaded four at a time");
+            uint2 prs[4];  // each group of four pairs is loaded before its first take
 #pragma unroll
             for (int k = 0; k < kBucketItems; ++k) {
+                if (k % 4 == 0) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t qe = (uint32_t)(k + e) * kThreads + tid;
+                        if (qe < t) prs[e] = bk.pairs[base + qe];
+                    }
+                }
                 const uint32_t q = (uint32_t)k * kThreads + tid;
                 bool valid = q < t;
                 uint32_t local = 0u;
                 if (valid) {
-                    const uint2 pr = bk.pairs[base + q];
+                    const uint2 pr = prs[k % 4];
                     local = pr.x - (uint32_t)cl;
                     s_who[q] = pr.y;
                     if (local >= w) {
